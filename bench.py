@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the hyper-connection mixing step on GB300.
+
+One step = one pass of the whole path over one batch of tokens:
+  hc_mixes_pre  (RMS statistic + mix projection + split/Sinkhorn + collapse)
+  hc_post       (expansion of a sublayer output back into the hc copies)
+with the sublayer's output taken as a synthetic bf16 N(0,1) tensor and the
+residual being the stream itself.  Inputs are resident in HBM when the timed
+region starts; `e2e` repeats the measurement through the same public calls
+with pinned HOST buffers, host<->device copies inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torch.distributed.run: every rank runs the same
+workload on its own GPU (weak scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "HC mix+Sinkhorn+pre+post tokens/s at d=5120,hc=4; % of HBM roofline"
+UNIT = "tokens/s"
+DESCR = {
+    "large": "large batched prefill: B=8, T=8192 (65,536 tokens), hc=4, d=5120, iters=20, "
+             "per-token stream scale log-uniform [1e-3, 1e3]",
+    "prefill": "prefill: B=1, T=4096 (4,096 tokens), hc=4, d=5120, iters=20",
+    "decode": "decode step: B=64, T=1 (64 tokens), hc=4, d=5120, iters=20",
+    "stress": "stress: B=4, T=16384 (65,536 tokens), hc=8, d=5120, iters=20",
+}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(DESCR), default="large")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ algorithmic bytes
+
+def bytes_mixes_pre(n, hc, d):
+    """x read once, y written once, pre/post/comb written once, W read once."""
+    mix = (2 + hc) * hc
+    return n * (hc * d * 2 + d * 2 + (2 * hc + hc * hc) * 4) + mix * hc * d * 4 + (3 + mix) * 4
+
+
+def bytes_post(n, hc, d):
+    """out and residual read, post/comb read, y written."""
+    return n * (d * 2 + hc * d * 2 + (hc + hc * hc) * 4 + hc * d * 2)
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+
+    def start(self):
+        try:
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        j = json.load(f)
+    rec = j.get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != rec.get("source_sha256_16"):
+        return None
+    return rec
+
+
+def cpu_baseline(wl, seconds):
+    """The float64 oracle, as it stands, on a bounded sample of the workload's
+    tokens (same recipe, drawn on the host), timed on this host's cores."""
+    import oracle
+    from sinkhorn_mixing_gb300 import inputs
+    p = inputs.make_params(wl)
+    w, sc, b = p["w"].numpy(), p["hc_scale"].numpy(), p["hc_base"].numpy()
+
+    def run(k):
+        s = inputs.make_streams(wl, n=k, device="cpu")
+        xb, ob = inputs.bf16_bits(s["x"]), inputs.bf16_bits(s["out"])
+        t0 = time.perf_counter()
+        oracle.chain(xb, w, sc, b, ob, None, wl.iters[0], wl.eps, wl.norm_eps)
+        return time.perf_counter() - t0
+
+    k = 16
+    dt = run(k)
+    k = max(16, min(wl.n, int(k * seconds / max(dt, 1e-3))))
+    dt = run(k)
+    return {"value": k / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of the %d tokens (same recipe, host-drawn), full path "
+                      "mixes->Sinkhorn->pre->post in float64, %.1f s" % (k, wl.n, dt)}
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return
+    import oracle
+    from sinkhorn_mixing_gb300 import inputs
+    p = inputs.make_params(wl)
+    w, sc, b = p["w"].numpy(), p["hc_scale"].numpy(), p["hc_base"].numpy()
+    budget = 90.0  # seconds for the whole warmup + timed run
+    s1 = inputs.make_streams(wl, n=8, device="cpu")
+    t0 = time.perf_counter()
+    oracle.chain(inputs.bf16_bits(s1["x"]), w, sc, b, inputs.bf16_bits(s1["out"]), None,
+                 wl.iters[0], wl.eps, wl.norm_eps)
+    per_tok = (time.perf_counter() - t0) / 8
+    k = int(max(1, min(4096, wl.n,
+                       budget / max(1, args.steps + args.warmup) / max(per_tok, 1e-9))))
+    s = inputs.make_streams(wl, n=k, device="cpu")
+    xb, ob = inputs.bf16_bits(s["x"]), inputs.bf16_bits(s["out"])
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.chain(xb, w, sc, b, ob, None, wl.iters[0], wl.eps, wl.norm_eps)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    val = k * args.steps / tot
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "tokens_per_step": k},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": "%d of the %d tokens per step, float64 oracle" % (k, wl.n)},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, wl, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+    import sinkhorn_mixing_gb300 as hc
+    from sinkhorn_mixing_gb300 import build, inputs
+
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n, H, d = wl.n, wl.hc, wl.d
+    iters = 20 if 20 in wl.iters else wl.iters[0]
+    s = inputs.make_streams(wl, device=dev)
+    p = inputs.make_params(wl, device=dev)
+    x, out = s["x"], s["out"]
+    pre = torch.empty((n, H), device=dev)
+    post = torch.empty((n, H), device=dev)
+    comb = torch.empty((n, H, H), device=dev)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    ys = torch.empty((n, H, d), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(max(256, hc.hc_workspace_bytes(n, H, d)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = x.numel() * 2 + out.numel() * 2
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def k1():
+        hc.hc_mixes_pre(x, p["w"], p["hc_scale"], p["hc_base"], iters, wl.eps, wl.norm_eps,
+                        pre=pre, post=post, comb=comb, y=y, workspace=wsp)
+
+    def k2():
+        hc.hc_post(out, x, post, comb, y=ys)
+
+    for _ in range(max(3, args.warmup)):
+        if flush is not None:
+            flush.zero_()
+        k1()
+        k2()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = hc.hc_launch_count()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        k1()
+        ev[i][1].record(stream)
+        k2()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    launches = hc.hc_launch_count() - launches0
+    clk = clocks.stop()
+    if ws > 1:
+        dist.barrier()
+    t1 = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    t2 = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    tot = t1 + t2
+    if ws > 1:
+        tt = torch.tensor([tot], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        tot = float(tt.item())
+    err = hc.hc_device_error(clear=True)
+    if err:
+        raise RuntimeError("device error word set: %#x" % err)
+
+    # ------------------------------------------------------------ e2e (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        xh = x.cpu().pin_memory()
+        oh = out.cpu().pin_memory()
+        yh = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        ysh = torch.empty(ys.shape, dtype=ys.dtype).pin_memory()
+        coef_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (pre, post, comb)]
+        h2d = xh.numel() * 2 + oh.numel() * 2
+        d2h = yh.numel() * 2 + ysh.numel() * 2 + sum(t.numel() * 4 for t in coef_h)
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            out.copy_(oh, non_blocking=True)
+            k1()
+            k2()
+            yh.copy_(y, non_blocking=True)
+            ysh.copy_(ys, non_blocking=True)
+            for h_, d_ in zip(coef_h, (pre, post, comb)):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        te = a.elapsed_time(b) / 1e3
+        if ws > 1:
+            tt = torch.tensor([te], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e2e = {"value": ws * n * args.e2e_steps / te, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    b1, b2 = bytes_mixes_pre(n, H, d), bytes_post(n, H, d)
+    a1, a2 = t1 / args.steps, t2 / args.steps
+    dom_is_post = a2 >= a1
+    kname = "hc_post" if dom_is_post else "hc_mixes_pre"
+    achieved = (b2 / a2 if dom_is_post else b1 / a1) / 1e9
+    tr = traffic_record(kname)
+    line = {
+        "metric": METRIC, "value": ws * n * args.steps / tot, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "tokens": n, "hc": H, "d": d,
+                   "iters": iters, "l2": ("flushed between steps (%d MB write)" %
+                                          (2 * L2_BYTES >> 20)) if flush is not None
+                   else "inputs larger than L2 (stream %.2f GB), no flush" % (x.numel() * 2 / 1e9),
+                   "parallelism": "replicas" if ws == 1 else "dp%d (token shards)" % ws},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": (tr["dram_bytes_per_launch"] if tr else None)},
+        "kernels": {
+            "hc_mixes_pre": {"us_per_launch": 1e6 * a1, "algorithmic_bytes": b1,
+                             "GBps": b1 / a1 / 1e9, "frac": b1 / a1 / 1e9 / peak},
+            "hc_post": {"us_per_launch": 1e6 * a2, "algorithmic_bytes": b2,
+                        "GBps": b2 / a2 / 1e9, "frac": b2 / a2 / 1e9 / peak},
+            "step_frac_of_hbm_roofline": (b1 + b2) / (a1 + a2) / 1e9 / peak,
+        },
+        "wall_s_timed": t_wall,
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    from sinkhorn_mixing_gb300 import inputs
+    wl = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, wl, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

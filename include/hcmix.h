@@ -1,0 +1,163 @@
+/*
+ * hcmix.h -- C ABI of libhcmix.so: hyper-connection (HC) residual mixing on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operations are those of the "DeepSeek V4.1" model-atlas pages:
+ *   hc_mixes           "Mix projection" page: formula for m and Block.hc_mixes
+ *                      (model.py 948-966)
+ *   hc_split_sinkhorn  "Reading weights" page: pre formula and the
+ *                      hc_split_sinkhorn kernel and wrapper (kernel.py 406-474)
+ *   hc_pre, hc_post    "Mix projection" page: Block.hc_pre, Block.hc_post
+ *   hc_mixes_pre       the first three fused: what one sublayer needs before
+ *                      it runs (Block docstring on the same page)
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *     library never allocates, frees or retains memory, and keeps no pointer
+ *     after a call returns.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and returns as soon as its kernels are enqueued.
+ *   - n is the flattened token count (the pages view [b, s, ...] tensors as
+ *     [n, ...]); hc is the number of residual copies; d the channel width.
+ *     F = hc*d features per token and mix_hc = (2+hc)*hc mix numbers.
+ *   - bf16 tensors are passed as their 16-bit patterns (uint16_t); float
+ *     tensors are IEEE binary32.  All tensors are dense, row-major, with the
+ *     layouts stated per function.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     call that returns an error has launched nothing.  n == 0 is a valid
+ *     no-op.  Supported: hc in {4, 8}; d > 0 with d % 8 == 0; every pointer
+ *     16-byte aligned; iters >= 1; eps >= 0; norm_eps >= 0.
+ *   - Outputs must not overlap inputs or each other, except that hc_post may
+ *     write y over residual exactly (y == residual).
+ *   - The library never aborts, exits or traps.  CUDA launch failures are
+ *     returned as HC_ERR_CUDA.  Kernels with bounded internal waits record a
+ *     timeout in a per-device error word that hc_device_error() reads.
+ */
+#ifndef HCMIX_H
+#define HCMIX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *hc_stream_t;
+
+typedef enum hc_status {
+    HC_OK = 0,
+    HC_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad iters/eps,
+                                overlapping buffers, workspace too small */
+    HC_ERR_UNSUPPORTED = 2,  /* hc not in {4, 8}, sizes beyond int64 range */
+    HC_ERR_MISALIGNED = 3,   /* d % 8 != 0 or a pointer not 16-byte aligned */
+    HC_ERR_CUDA = 4          /* a CUDA runtime call or launch failed */
+} hc_status;
+
+#define HCMIX_ABI_VERSION 1
+
+/* Static, NUL-terminated description of a status code.  Never NULL. */
+const char *hc_status_string(hc_status s);
+
+/* HCMIX_ABI_VERSION of the built library. */
+int hc_abi_version(void);
+
+/*
+ * hc_mixes -- mix projection ("Mix projection" page, formula for m):
+ *   r_t          = 1 / sqrt( mean_f x_{t,f}^2 + norm_eps )
+ *   mixes_{t,i}  = r_t * sum_f x_{t,f} * w_mix_{i,f}
+ * with x flattened per token, f = j*d + c.  Accumulation is binary32.
+ *   x      [n, hc, d] bf16 (in)
+ *   w_mix  [mix_hc, hc*d] float (in) -- the hc_{attn,ffn}_fn parameter
+ *   mixes  [n, mix_hc] float (out)
+ */
+hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps,
+                   const uint16_t *x, const float *w_mix, float *mixes,
+                   hc_stream_t stream);
+
+/*
+ * hc_split_sinkhorn -- split of the mixes and Sinkhorn normalisation
+ * ("Reading weights" page, pre formula and the hc_split_sinkhorn kernel):
+ *   pre_j   = sigmoid(m_j * s0 + b_j) + eps
+ *   post_j  = 2 * sigmoid(m_{hc+j} * s1 + b_{hc+j})
+ *   L_{j,k} = m_{2hc+j*hc+k} * s2 + b_{2hc+j*hc+k}
+ *   comb    = softmax over k of L, + eps; then a column step; then iters-1
+ *             rounds of (row step, column step), where a step divides each
+ *             entry by (its row or column sum + eps).
+ *   mixes    [n, mix_hc] float (in)
+ *   hc_scale [3] float (in) = (s0, s1, s2);  hc_base [mix_hc] float (in) = b
+ *   pre, post [n, hc] float (out);  comb [n, hc, hc] float (out), [t, j, k]
+ * iters < 1 is rejected (HC_ERR_INVALID_ARG).
+ */
+hc_status hc_split_sinkhorn(int64_t n, int hc, int iters, float eps,
+                            const float *mixes, const float *hc_scale,
+                            const float *hc_base, float *pre, float *post,
+                            float *comb, hc_stream_t stream);
+
+/*
+ * hc_pre -- collapse of the copies ("Mix projection" page, Block.hc_pre):
+ *   y_{t,c} = sum_j pre_{t,j} * x_{t,j,c}, binary32 accumulation, stored as
+ *   bf16 rounded to nearest-even.
+ *   x [n, hc, d] bf16 (in);  pre [n, hc] float (in);  y [n, d] bf16 (out)
+ */
+hc_status hc_pre(int64_t n, int hc, int64_t d, const uint16_t *x,
+                 const float *pre, uint16_t *y, hc_stream_t stream);
+
+/*
+ * hc_post -- expansion back to hc copies ("Mix projection" page,
+ * Block.hc_post):
+ *   y_{t,k,c} = post_{t,k} * out_{t,c} + sum_j comb_{t,j,k} * residual_{t,j,c}
+ * (the sum runs over the FIRST comb index), binary32 arithmetic, stored as
+ * bf16 rounded to nearest-even.
+ *   out [n, d] bf16 (in);  residual [n, hc, d] bf16 (in)
+ *   post [n, hc] float (in);  comb [n, hc, hc] float (in)
+ *   y [n, hc, d] bf16 (out); y == residual (in place) is allowed.
+ */
+hc_status hc_post(int64_t n, int hc, int64_t d, const uint16_t *out,
+                  const uint16_t *residual, const float *post,
+                  const float *comb, uint16_t *y, hc_stream_t stream);
+
+/*
+ * hc_mixes_pre -- hc_mixes, hc_split_sinkhorn and hc_pre in one call, i.e.
+ * everything a sublayer needs from the stream before it runs (Block
+ * docstring, "Mix projection" page).  Results equal those of the three
+ * separate calls up to binary32 rounding order.
+ *   x [n, hc, d] bf16 (in); w_mix, hc_scale, hc_base as above (in)
+ *   mixes [n, mix_hc] float (out, may be NULL)
+ *   pre, post [n, hc], comb [n, hc, hc] float (out)
+ *   y [n, d] bf16 (out) -- the collapsed sublayer input
+ *   workspace: device scratch of at least hc_workspace_bytes(n, hc, d)
+ *   bytes, 256-byte aligned, not shared with another call in flight.  It is
+ *   required when mixes is NULL (it may then hold the mix numbers between
+ *   the kernels of the general path) and ignored otherwise (may be NULL).
+ */
+hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps,
+                       float norm_eps, const uint16_t *x, const float *w_mix,
+                       const float *hc_scale, const float *hc_base,
+                       float *mixes, float *pre, float *post, float *comb,
+                       uint16_t *y, void *workspace, size_t workspace_bytes,
+                       hc_stream_t stream);
+
+/* Scratch bytes hc_mixes_pre may need for these sizes when mixes is NULL
+ * (n * mix_hc floats, rounded up to 256 bytes; 0 for n == 0 or invalid
+ * sizes).  Pure host function; the value depends only on its arguments. */
+size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
+
+/*
+ * hc_device_error -- reads the error word of the current CUDA device:
+ * bit 0 set = a kernel gave up on a bounded wait (its outputs for the
+ * affected tile are not valid).  Synchronises the device.  With clear != 0
+ * the word is reset to 0 afterwards.  flags may be NULL (then only clears).
+ */
+hc_status hc_device_error(unsigned int *flags, int clear);
+
+/* Number of kernels this library has enqueued in this process (all devices,
+ * all threads) since it was loaded.  Host-only counter for diagnostics. */
+uint64_t hc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HCMIX_H */

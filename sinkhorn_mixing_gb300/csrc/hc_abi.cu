@@ -1,0 +1,273 @@
+// hc_abi.cu -- the extern "C" entry points of libhcmix.so: host-side argument
+// validation, path selection and launch.  Nothing here allocates memory.
+#include <math.h>
+#include <atomic>
+#include <mutex>
+
+#include "../../include/hcmix.h"
+#include "hc_fused.h"
+#include "hc_internal.h"
+
+namespace hc {
+
+// Per-device error word: kernels with bounded waits set bits here instead of
+// trapping.  Read and cleared through hc_device_error().
+__device__ unsigned int g_err_word;
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_have[kMaxDevices];
+}  // namespace
+
+void count_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+cudaError_t device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_have[dev]) {
+        DeviceInfo di;
+        di.device = dev;
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_err_word);
+        if (e != cudaSuccess) return e;
+        di.err_word = static_cast<unsigned int *>(p);
+        g_info[dev] = di;
+        g_have[dev] = true;
+    }
+    *out = g_info[dev];
+    return cudaSuccess;
+}
+
+}  // namespace hc
+
+namespace {
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+Range rng(const void *p, uint64_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + (uintptr_t)bytes};
+}
+bool overlap(const Range &a, const Range &b) {
+    return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo;
+}
+
+bool finite_nonneg(float v) { return v >= 0.0f && v < INFINITY; }
+
+// Shape checks shared by the entry points that take d.
+hc_status check_shape(int64_t n, int hc, int64_t d) {
+    if (n < 0 || d <= 0) return HC_ERR_INVALID_ARG;
+    if (hc != 4 && hc != 8) return HC_ERR_UNSUPPORTED;
+    if (d % 8 != 0) return HC_ERR_MISALIGNED;
+    // keep every byte count well inside int64: n <= 2^40, d <= 2^24
+    if (n > (int64_t(1) << 40) || d > (int64_t(1) << 24)) return HC_ERR_UNSUPPORTED;
+    return HC_OK;
+}
+
+hc_status check_hc_n(int64_t n, int hc) {
+    if (n < 0) return HC_ERR_INVALID_ARG;
+    if (hc != 4 && hc != 8) return HC_ERR_UNSUPPORTED;
+    if (n > (int64_t(1) << 40)) return HC_ERR_UNSUPPORTED;
+    return HC_OK;
+}
+
+hc_status ptrs_ok(std::initializer_list<const void *> ps) {
+    for (const void *p : ps)
+        if (p == nullptr) return HC_ERR_INVALID_ARG;
+    for (const void *p : ps)
+        if (!al16(p)) return HC_ERR_MISALIGNED;
+    return HC_OK;
+}
+
+// Every output range must be disjoint from every other listed range.
+bool disjoint(std::initializer_list<Range> outs, std::initializer_list<Range> ins) {
+    for (auto a = outs.begin(); a != outs.end(); ++a) {
+        for (auto b = a + 1; b != outs.end(); ++b)
+            if (overlap(*a, *b)) return false;
+        for (const Range &b : ins)
+            if (overlap(*a, b)) return false;
+    }
+    return true;
+}
+
+hc_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HC_OK : HC_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *hc_status_string(hc_status s) {
+    switch (s) {
+        case HC_OK: return "HC_OK: success";
+        case HC_ERR_INVALID_ARG:
+            return "HC_ERR_INVALID_ARG: null pointer, negative size, bad iters/eps, "
+                   "overlapping buffers or workspace too small";
+        case HC_ERR_UNSUPPORTED: return "HC_ERR_UNSUPPORTED: hc must be 4 or 8; sizes too large";
+        case HC_ERR_MISALIGNED:
+            return "HC_ERR_MISALIGNED: d must be a multiple of 8 and pointers 16-byte aligned";
+        case HC_ERR_CUDA: return "HC_ERR_CUDA: a CUDA runtime call or kernel launch failed";
+    }
+    return "unknown hc_status";
+}
+
+int hc_abi_version(void) { return HCMIX_ABI_VERSION; }
+
+uint64_t hc_launch_count(void) { return hc::g_launches.load(std::memory_order_relaxed); }
+
+size_t hc_workspace_bytes(int64_t n, int hc, int64_t d) {
+    if (check_shape(n, hc, d) != HC_OK || n == 0) return 0;
+    const uint64_t b = (uint64_t)n * (uint64_t)((2 + hc) * hc) * 4u;
+    return (size_t)((b + 255u) / 256u * 256u);
+}
+
+hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                   const float *w_mix, float *mixes, hc_stream_t stream) {
+    hc_status st = check_shape(n, hc, d);
+    if (st != HC_OK) return st;
+    if (!finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({x, w_mix, mixes})) != HC_OK) return st;
+    const int mix = (2 + hc) * hc;
+    const uint64_t F = (uint64_t)hc * d;
+    if (!disjoint({rng(mixes, (uint64_t)n * mix * 4)},
+                  {rng(x, (uint64_t)n * F * 2), rng(w_mix, (uint64_t)mix * F * 4)}))
+        return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    cudaError_t e = hc::device_info(&di);
+    if (e != cudaSuccess) return HC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hc::fused_supported(hc, d, di)) {
+        return from_cuda(hc::launch_fused(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
+                                          w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
+                                          nullptr, nullptr, di, s));
+    }
+    return from_cuda(hc::launch_mixes(n, hc, d, norm_eps, x, w_mix, mixes, di, s));
+}
+
+hc_status hc_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,
+                            const float *hc_scale, const float *hc_base, float *pre,
+                            float *post, float *comb, hc_stream_t stream) {
+    hc_status st = check_hc_n(n, hc);
+    if (st != HC_OK) return st;
+    if (iters < 1 || !finite_nonneg(eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({mixes, hc_scale, hc_base, pre, post, comb})) != HC_OK) return st;
+    const uint64_t mix = (uint64_t)(2 + hc) * hc;
+    if (!disjoint({rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
+                   rng(comb, n * (uint64_t)hc * hc * 4ull)},
+                  {rng(mixes, n * mix * 4ull), rng(hc_scale, 12), rng(hc_base, mix * 4)}))
+        return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    return from_cuda(hc::launch_split_sinkhorn(n, hc, iters, eps, mixes, hc_scale, hc_base, pre,
+                                               post, comb, di,
+                                               reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hc_status hc_pre(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre, uint16_t *y,
+                 hc_stream_t stream) {
+    hc_status st = check_shape(n, hc, d);
+    if (st != HC_OK) return st;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({x, pre, y})) != HC_OK) return st;
+    if (!disjoint({rng(y, (uint64_t)n * d * 2)},
+                  {rng(x, (uint64_t)n * hc * d * 2), rng(pre, (uint64_t)n * hc * 4)}))
+        return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    return from_cuda(
+        hc::launch_pre(n, hc, d, x, pre, y, di, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hc_status hc_post(int64_t n, int hc, int64_t d, const uint16_t *out, const uint16_t *residual,
+                  const float *post, const float *comb, uint16_t *y, hc_stream_t stream) {
+    hc_status st = check_shape(n, hc, d);
+    if (st != HC_OK) return st;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({out, residual, post, comb, y})) != HC_OK) return st;
+    const uint64_t ybytes = (uint64_t)n * hc * d * 2;
+    const Range ry = rng(y, ybytes), rr = rng(residual, ybytes);
+    const bool in_place = (const void *)y == (const void *)residual;
+    if (!in_place && overlap(ry, rr)) return HC_ERR_INVALID_ARG;
+    if (!disjoint({ry}, {rng(out, (uint64_t)n * d * 2), rng(post, (uint64_t)n * hc * 4),
+                         rng(comb, (uint64_t)n * hc * hc * 4)}))
+        return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    return from_cuda(hc::launch_post(n, hc, d, out, residual, post, comb, y, di,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                       const uint16_t *x, const float *w_mix, const float *hc_scale,
+                       const float *hc_base, float *mixes, float *pre, float *post, float *comb,
+                       uint16_t *y, void *workspace, size_t workspace_bytes,
+                       hc_stream_t stream) {
+    hc_status st = check_shape(n, hc, d);
+    if (st != HC_OK) return st;
+    if (iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({x, w_mix, hc_scale, hc_base, pre, post, comb, y})) != HC_OK) return st;
+    if (mixes != nullptr && !al16(mixes)) return HC_ERR_MISALIGNED;
+    const uint64_t mix = (uint64_t)(2 + hc) * hc, F = (uint64_t)hc * d;
+    const Range rmix = mixes ? rng(mixes, n * mix * 4) : Range{0, 0};
+    if (!disjoint({rmix, rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
+                   rng(comb, n * (uint64_t)hc * hc * 4ull), rng(y, (uint64_t)n * d * 2)},
+                  {rng(x, n * F * 2), rng(w_mix, mix * F * 4), rng(hc_scale, 12),
+                   rng(hc_base, mix * 4)}))
+        return HC_ERR_INVALID_ARG;
+    // Without `mixes` the workspace must be there (the general path keeps
+    // the mix numbers in it between its stages).
+    float *m = mixes;
+    if (m == nullptr) {
+        if (workspace == nullptr || workspace_bytes < hc_workspace_bytes(n, hc, d))
+            return HC_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HC_ERR_MISALIGNED;
+        m = static_cast<float *>(workspace);
+        const Range rw = rng(workspace, workspace_bytes);
+        if (!disjoint({rw}, {rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
+                             rng(comb, n * (uint64_t)hc * hc * 4ull),
+                             rng(y, (uint64_t)n * d * 2), rng(x, n * F * 2),
+                             rng(w_mix, mix * F * 4), rng(hc_scale, 12), rng(hc_base, mix * 4)}))
+            return HC_ERR_INVALID_ARG;
+    }
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hc::fused_supported(hc, d, di)) {
+        return from_cuda(hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
+                                          hc_base, mixes, pre, post, comb, y, di, s));
+    }
+    // General path: three kernels, the mix numbers passing through m.
+    cudaError_t e = hc::launch_mixes(n, hc, d, norm_eps, x, w_mix, m, di, s);
+    if (e == cudaSuccess)
+        e = hc::launch_split_sinkhorn(n, hc, iters, eps, m, hc_scale, hc_base, pre, post, comb,
+                                      di, s);
+    if (e == cudaSuccess) e = hc::launch_pre(n, hc, d, x, pre, y, di, s);
+    return from_cuda(e);
+}
+
+hc_status hc_device_error(unsigned int *flags, int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return HC_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, hc::g_err_word, sizeof v) != cudaSuccess) return HC_ERR_CUDA;
+    if (flags) *flags = v;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(hc::g_err_word, &z, sizeof z) != cudaSuccess) return HC_ERR_CUDA;
+    }
+    return HC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// hc_common.cuh -- device helpers shared by the HC mixing kernels.
+//
+// bf16 <-> binary32 conversion, 16-byte streaming loads and stores, and the
+// per-token split + Sinkhorn normalisation ("Reading weights" page, pre
+// formula and the hc_split_sinkhorn kernel), written once so that the
+// standalone and the fused kernels compute identical coefficients.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hc {
+
+// Error word bits (per device, read by hc_device_error).
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+// ---------------------------------------------------------------- bf16
+
+// Two bf16 values packed in a 32-bit word -> two floats (exact).
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Two floats -> two bf16 (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// 8 bf16 in a uint4 -> 8 floats.
+__device__ __forceinline__ void unpack8(const uint4 &v, float f[8]) {
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// Streaming (evict-first) 16-byte global load/store.  Plain coherent loads:
+// safe also when the same kernel later writes the location (in-place post).
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// ------------------------------------------------- split + Sinkhorn
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// One token.  m: the token's (2+HC)*HC mix numbers; s0..s2 = hc_scale;
+// base = hc_base.  Outputs pre[HC], post[HC], C[HC][HC] (row j, column k).
+//   pre_j  = sigmoid(m_j s0 + b_j) + eps
+//   post_j = 2 sigmoid(m_{HC+j} s1 + b_{HC+j})
+//   L_jk   = m_{2HC+j HC+k} s2 + b_{2HC+j HC+k}
+//   C = rowsoftmax(L) + eps; column step; (iters-1) x (row step, column step)
+// A step divides by (sum + eps); the division is done as a multiplication by
+// the correctly rounded reciprocal of the shared denominator.
+template <int HC, typename MixFn, typename BaseFn>
+__device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float s0, float s1,
+                                                     float s2, int iters, float eps,
+                                                     float pre[HC], float post[HC],
+                                                     float C[HC][HC]) {
+#pragma unroll
+    for (int j = 0; j < HC; ++j) pre[j] = sigmoidf_(fmaf(m(j), s0, base(j))) + eps;
+#pragma unroll
+    for (int j = 0; j < HC; ++j) post[j] = 2.0f * sigmoidf_(fmaf(m(HC + j), s1, base(HC + j)));
+#pragma unroll
+    for (int j = 0; j < HC; ++j)
+#pragma unroll
+        for (int k = 0; k < HC; ++k)
+            C[j][k] = fmaf(m(2 * HC + j * HC + k), s2, base(2 * HC + j * HC + k));
+
+    // row softmax (max-subtracted, plain row sum), then + eps
+#pragma unroll
+    for (int j = 0; j < HC; ++j) {
+        float mx = C[j][0];
+#pragma unroll
+        for (int k = 1; k < HC; ++k) mx = fmaxf(mx, C[j][k]);
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {
+            C[j][k] = expf(C[j][k] - mx);
+            s += C[j][k];
+        }
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int k = 0; k < HC; ++k) C[j][k] = fmaf(C[j][k], inv, eps);
+    }
+    // column step
+#pragma unroll
+    for (int k = 0; k < HC; ++k) {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < HC; ++j) s += C[j][k];
+        const float inv = 1.0f / (s + eps);
+#pragma unroll
+        for (int j = 0; j < HC; ++j) C[j][k] *= inv;
+    }
+    for (int it = 1; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < HC; ++j) {  // row step
+            float s = 0.0f;
+#pragma unroll
+            for (int k = 0; k < HC; ++k) s += C[j][k];
+            const float inv = 1.0f / (s + eps);
+#pragma unroll
+            for (int k = 0; k < HC; ++k) C[j][k] *= inv;
+        }
+#pragma unroll
+        for (int k = 0; k < HC; ++k) {  // column step
+            float s = 0.0f;
+#pragma unroll
+            for (int j = 0; j < HC; ++j) s += C[j][k];
+            const float inv = 1.0f / (s + eps);
+#pragma unroll
+            for (int j = 0; j < HC; ++j) C[j][k] *= inv;
+        }
+    }
+}
+
+}  // namespace hc

@@ -1,0 +1,24 @@
+// hc_fused.h -- the fused mix projection + Sinkhorn + collapse path
+// (tensor-core projection, thread-block clusters), behind hc_mixes_pre and
+// hc_mixes.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hc_internal.h"
+
+namespace hc {
+
+// True when the fused kernel handles this (hc, d) on the current device.
+bool fused_supported(int hc, int64_t d, const DeviceInfo &di);
+
+// pre == nullptr selects the projection-only mode (hc_mixes): only `mixes`
+// is written.  Otherwise pre, post, comb and y are written, and mixes when
+// it is not null.
+cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                         const uint16_t *x, const float *w, const float *scale,
+                         const float *base, float *mixes, float *pre, float *post, float *comb,
+                         uint16_t *y, const DeviceInfo &di, cudaStream_t s);
+
+}  // namespace hc

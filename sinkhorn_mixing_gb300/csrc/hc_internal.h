@@ -1,0 +1,44 @@
+// hc_internal.h -- launchers behind the C ABI (not part of the public ABI).
+// Arguments are already validated by hc_abi.cu when these are called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hc {
+
+struct DeviceInfo {
+    int device;
+    int sms;
+    unsigned int *err_word;  // device address of this device's error word
+};
+
+// Current device's SM count and error-word address (cached per device).
+cudaError_t device_info(DeviceInfo *out);
+
+// Adds k to the process-wide count of enqueued kernels (hc_launch_count).
+void count_launches(int k);
+
+// cudaGetLastError() after a launch, counting the launch when it succeeded.
+inline cudaError_t launched(int k = 1) {
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(k);
+    return e;
+}
+
+cudaError_t launch_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                         const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s);
+
+cudaError_t launch_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,
+                                  const float *scale, const float *base, float *pre,
+                                  float *post, float *comb, const DeviceInfo &di,
+                                  cudaStream_t s);
+
+cudaError_t launch_pre(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
+                       uint16_t *y, const DeviceInfo &di, cudaStream_t s);
+
+cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
+                        const uint16_t *res, const float *post, const float *comb, uint16_t *y,
+                        const DeviceInfo &di, cudaStream_t s);
+
+}  // namespace hc

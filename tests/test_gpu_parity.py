@@ -1,0 +1,323 @@
+"""GPU parity: every entry point of libhcmix.so, called through the C ABI
+(via the ctypes binding), against the float64 oracle on the same seeded
+inputs.  Stage parity: each stage's oracle is fed the GPU's own inputs to
+that stage (the GPU mix numbers go into the oracle's Sinkhorn, the GPU
+coefficients into the oracle's collapse/expansion), so each tolerance bounds
+one stage's arithmetic.  At full sizes the oracle checks a seeded sample of
+tokens (first, last, middle and random ones).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import compare
+from sinkhorn_mixing_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+WL = inputs.WORKLOADS
+
+
+@pytest.fixture(scope="module")
+def hc():
+    from sinkhorn_mixing_gb300 import build
+    build.build()
+    import sinkhorn_mixing_gb300 as m
+    m.hc_device_error(clear=True)
+    yield m
+    torch.cuda.synchronize()
+    assert m.hc_device_error(clear=True) == 0
+
+
+def sample_idx(n, k=192, seed=0):
+    if n <= k:
+        return np.arange(n)
+    r = np.random.default_rng(seed)
+    idx = np.concatenate([[0, 1, n // 2, n - 2, n - 1], r.choice(n, k - 5, replace=False)])
+    return np.unique(idx)
+
+
+def bits(t):
+    return inputs.bf16_bits(t)
+
+
+def np64(t):
+    return t.detach().cpu().double().numpy()
+
+
+def params(wl, dev="cuda", param_set=0):
+    return inputs.make_params(wl, param_set, device=dev)
+
+
+def streams(wl, n=None, dev="cuda"):
+    return inputs.make_streams(wl, n=n, device=dev)
+
+
+def check_split(m_gpu, pre, post, comb, p, hc, iters, eps, idx):
+    o_pre, o_post, o_comb = oracle.hc_split_sinkhorn(
+        np64(m_gpu)[idx], p["hc_scale"].cpu().numpy(), p["hc_base"].cpu().numpy(), hc, iters,
+        eps)
+    compare.check_abs(np64(pre)[idx], o_pre, 1e-5, "pre")
+    compare.check_abs(np64(post)[idx], o_post, 1e-5, "post")
+    compare.check_abs(np64(comb)[idx], o_comb, 1e-5, "comb")
+
+
+# ------------------------------------------------------------------ hc_post
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large", "stress"])
+def test_post_parity(hc, name):
+    wl = WL[name]
+    s = streams(wl)
+    n = wl.n
+    g = torch.Generator(device="cuda").manual_seed(7)
+    post = torch.rand((n, wl.hc), device="cuda", generator=g) * 2
+    comb = torch.rand((n, wl.hc, wl.hc), device="cuda", generator=g)
+    y = hc.hc_post(s["out"], s["residual"], post, comb)
+    torch.cuda.synchronize()
+    idx = sample_idx(n)
+    want, _, mag = oracle.hc_post(bits(s["out"][idx]), bits(s["residual"][idx]),
+                                  np64(post)[idx], np64(comb)[idx])
+    compare.check_bf16(bits(y[idx]), want, mag, wl.hc + 1, "hc_post")
+
+
+def test_post_in_place_and_ragged(hc):
+    wl = WL["tiny"]
+    for n, d in ((1, 8), (3, 24), (37, 136)):
+        g = torch.Generator(device="cuda").manual_seed(n)
+        res = torch.randn((n, 4, d), device="cuda", generator=g).to(torch.bfloat16)
+        out = torch.randn((n, d), device="cuda", generator=g).to(torch.bfloat16)
+        post = torch.rand((n, 4), device="cuda", generator=g) * 2
+        comb = torch.rand((n, 4, 4), device="cuda", generator=g)
+        want, _, mag = oracle.hc_post(bits(out), bits(res), np64(post), np64(comb))
+        y_sep = hc.hc_post(out, res, post, comb)
+        hc.hc_post(out, res, post, comb, y=res)  # in place
+        torch.cuda.synchronize()
+        assert torch.equal(y_sep, res)
+        compare.check_bf16(bits(res), want, mag, 5, "hc_post in place")
+
+
+# ------------------------------------------------------------------- hc_pre
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large", "stress"])
+def test_pre_parity(hc, name):
+    wl = WL[name]
+    s = streams(wl)
+    n = wl.n
+    g = torch.Generator(device="cuda").manual_seed(8)
+    pre = torch.rand((n, wl.hc), device="cuda", generator=g) + 1e-6
+    y = hc.hc_pre(s["x"], pre)
+    torch.cuda.synchronize()
+    idx = sample_idx(n)
+    want, _, mag = oracle.hc_pre(bits(s["x"][idx]), np64(pre)[idx])
+    compare.check_bf16(bits(y[idx]), want, mag, wl.hc, "hc_pre")
+
+
+def test_pre_equal_weights_is_mean(hc):
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn((50, 4, 40), device="cuda", generator=g).to(torch.bfloat16)
+    y = hc.hc_pre(x, torch.full((50, 4), 0.25, device="cuda"))
+    want = oracle.bf16_bits_to_f64(bits(x)).mean(axis=1)
+    compare.check_bf16(bits(y), want, np.abs(oracle.bf16_bits_to_f64(bits(x))).sum(1) / 4, 4,
+                       "mean")
+
+
+# -------------------------------------------------------- hc_split_sinkhorn
+
+@pytest.mark.parametrize("name,iters", [("tiny", 20), ("decode", 20), ("large", 20),
+                                        ("stress", 1), ("stress", 20), ("stress", 50)])
+def test_split_sinkhorn_parity(hc, name, iters):
+    wl = WL[name]
+    n = wl.n
+    p = params(wl)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    mixes = torch.randn((n, wl.mix_hc), device="cuda", generator=g)
+    pre, post, comb = hc.hc_split_sinkhorn(mixes, p["hc_scale"], p["hc_base"], wl.hc, iters,
+                                           wl.eps)
+    torch.cuda.synchronize()
+    idx = np.arange(n) if n <= 8192 else sample_idx(n, 8192)
+    check_split(mixes, pre, post, comb, p, wl.hc, iters, wl.eps, idx)
+    assert torch.all(pre > 0) and torch.all(pre <= 1 + 2e-6)
+    assert torch.all(post >= 0) and torch.all(post <= 2)
+
+
+# ----------------------------------------------------------------- hc_mixes
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "large", "stress"])
+def test_mixes_parity(hc, name):
+    wl = WL[name]
+    s = streams(wl)
+    p = params(wl)
+    m = hc.hc_mixes(s["x"], p["w"], wl.norm_eps)
+    torch.cuda.synchronize()
+    idx = sample_idx(wl.n, 96)
+    want = oracle.hc_mixes(bits(s["x"][idx]), p["w"].cpu().numpy(), wl.norm_eps)
+    compare.check_mixes(np64(m)[idx], want)
+
+
+def test_mixes_power_of_two_scaling_invariance(hc):
+    wl = WL["prefill"]
+    s = streams(wl, n=256)
+    p = params(wl)
+    m1 = hc.hc_mixes(s["x"], p["w"])
+    m2 = hc.hc_mixes((s["x"].float() * 8).to(torch.bfloat16), p["w"])
+    torch.testing.assert_close(m2, m1, rtol=0, atol=2e-5)
+
+
+# ------------------------------------------------------------- hc_mixes_pre
+
+@pytest.mark.parametrize("name,iters", [("tiny", 20), ("decode", 20), ("prefill", 20),
+                                        ("large", 20), ("stress", 1), ("stress", 20),
+                                        ("stress", 50)])
+def test_mixes_pre_parity(hc, name, iters):
+    wl = WL[name]
+    s = streams(wl)
+    p = params(wl)
+    y, pre, post, comb, m = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"], iters,
+                                            wl.eps, wl.norm_eps, want_mixes=True)
+    torch.cuda.synchronize()
+    idx = sample_idx(wl.n, 96)
+    xb = bits(s["x"][idx])
+    compare.check_mixes(np64(m)[idx], oracle.hc_mixes(xb, p["w"].cpu().numpy(), wl.norm_eps))
+    check_split(m, pre, post, comb, p, wl.hc, iters, wl.eps, idx)
+    want, _, mag = oracle.hc_pre(xb, np64(pre)[idx])
+    compare.check_bf16(bits(y[idx]), want, mag, wl.hc, "hc_mixes_pre y")
+
+
+def test_mixes_pre_without_mixes_matches_with(hc):
+    wl = WL["prefill"]
+    s = streams(wl, n=300)
+    p = params(wl)
+    a = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"], want_mixes=True)
+    b = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"], want_mixes=False)
+    assert b[4] is None
+    for u, v in zip(a[:4], b[:4]):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("n,hcm,d", [(1, 4, 8), (3, 4, 72), (33, 4, 5120), (31, 8, 64),
+                                     (129, 4, 1024)])
+def test_mixes_pre_ragged_shapes(hc, n, hcm, d):
+    g = torch.Generator(device="cuda").manual_seed(n * 131 + d)
+    x = torch.randn((n, hcm, d), device="cuda", generator=g).to(torch.bfloat16)
+    mix = (2 + hcm) * hcm
+    w = torch.randn((mix, hcm * d), device="cuda", generator=g) / (hcm * d) ** 0.5
+    scale = torch.rand(3, device="cuda", generator=g) * 1.5 + 0.5
+    base = torch.randn(mix, device="cuda", generator=g)
+    y, pre, post, comb, m = hc.hc_mixes_pre(x, w, scale, base, want_mixes=True)
+    torch.cuda.synchronize()
+    compare.check_mixes(np64(m), oracle.hc_mixes(bits(x), w.cpu().numpy()))
+    pp = dict(hc_scale=scale, hc_base=base)
+    check_split(m, pre, post, comb, pp, hcm, 20, 1e-6, np.arange(n))
+    want, _, mag = oracle.hc_pre(bits(x), np64(pre))
+    compare.check_bf16(bits(y), want, mag, hcm, "y")
+
+
+def test_zero_token_uses_base_only(hc):
+    wl = WL["decode"]
+    p = params(wl)
+    x = torch.zeros((5, 4, 5120), dtype=torch.bfloat16, device="cuda")
+    y, pre, post, comb, m = hc.hc_mixes_pre(x, p["w"], p["hc_scale"], p["hc_base"],
+                                            want_mixes=True)
+    torch.cuda.synchronize()
+    assert torch.all(m == 0)
+    assert torch.all(y == 0)
+    b = p["hc_base"].cpu().double().numpy()
+    o_pre, o_post, o_comb = oracle.hc_split_sinkhorn(np.zeros((5, 24)),
+                                                     p["hc_scale"].cpu().numpy(), b, 4, 20, 1e-6)
+    compare.check_abs(np64(pre), o_pre, 1e-5, "pre")
+    compare.check_abs(np64(post), o_post, 1e-5, "post")
+    compare.check_abs(np64(comb), o_comb, 1e-5, "comb")
+
+
+def test_comb_cross_ratios_match_softmax_plus_eps(hc):
+    # every Sinkhorn step is a diagonal scaling: cross-ratios are those of
+    # softmax(L) + eps, computed here in double from the GPU's own mixes
+    wl = WL["prefill"]
+    s = streams(wl, n=512)
+    p = params(wl)
+    y, pre, post, comb, m = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"],
+                                            want_mixes=True)
+    torch.cuda.synchronize()
+    sc = p["hc_scale"].cpu().double().numpy()
+    b = p["hc_base"].cpu().double().numpy()
+    L = (np64(m)[:, 8:] * sc[2] + b[8:]).reshape(-1, 4, 4)
+    A = np.exp(L - L.max(-1, keepdims=True))
+    A = A / A.sum(-1, keepdims=True) + 1e-6
+    C = np64(comb)
+    for (j, k, j2, k2) in ((0, 0, 1, 1), (0, 1, 2, 3), (1, 2, 3, 0)):
+        rc = C[:, j, k] * C[:, j2, k2] / (C[:, j, k2] * C[:, j2, k])
+        ra = A[:, j, k] * A[:, j2, k2] / (A[:, j, k2] * A[:, j2, k])
+        np.testing.assert_allclose(rc, ra, rtol=2e-3)
+
+
+# ---------------------------------------------------------------- the chain
+
+def test_full_chain_tiny_end_to_end(hc):
+    wl = WL["tiny"]
+    s = streams(wl)
+    p = params(wl)
+    y, pre, post, comb, m = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"],
+                                            want_mixes=True)
+    out = s["out"]
+    y_post = hc.hc_post(out, s["residual"], post, comb)
+    torch.cuda.synchronize()
+    ref = oracle.chain(bits(s["x"]), p["w"].cpu().numpy(), p["hc_scale"].cpu().numpy(),
+                       p["hc_base"].cpu().numpy(), bits(out), bits(s["residual"]))
+    compare.check_mixes(np64(m), ref["mixes"])
+    for name, got in (("pre", pre), ("post", post), ("comb", comb)):
+        compare.check_abs(np64(got), ref[name], 1e-4, name + " end to end")
+    for got, want in ((y, ref["y_pre"]), (y_post, ref["y_post"])):
+        g = oracle.bf16_bits_to_f64(bits(got))
+        np.testing.assert_allclose(g, want, rtol=2 ** -7, atol=1e-3)
+
+
+def test_guard_bytes_untouched(hc):
+    n, d = 37, 136
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn((n, 4, d), device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn((24, 4 * d), device="cuda", generator=g) / (4 * d) ** 0.5
+    scale = torch.ones(3, device="cuda")
+    base = torch.zeros(24, device="cuda")
+    pad = 64
+
+    def padded(shape, dtype):
+        numel = int(np.prod(shape))
+        buf = torch.full((numel + 2 * pad,), 77, dtype=dtype, device="cuda")
+        return buf, buf[pad:pad + numel].view(shape)
+
+    bufs = [padded((n, 24), torch.float32), padded((n, 4), torch.float32),
+            padded((n, 4), torch.float32), padded((n, 4, 4), torch.float32),
+            padded((n, d), torch.bfloat16), padded((n, 4, d), torch.bfloat16)]
+    (bm, m), (bp, pre), (bq, post), (bc, comb), (by, y), (bz, z) = bufs
+    hc.hc_mixes_pre(x, w, scale, base, mixes=m, pre=pre, post=post, comb=comb, y=y)
+    hc.hc_post(y, x, post, comb, y=z)
+    torch.cuda.synchronize()
+    for buf, _ in bufs:
+        assert torch.all(buf[:pad] == 77) and torch.all(buf[-pad:] == 77)
+
+
+def test_runs_on_a_side_stream(hc):
+    wl = WL["tiny"]
+    s = streams(wl)
+    p = params(wl)
+    ref = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"])
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        got = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"])
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    for u, v in zip(ref[:4], got[:4]):
+        assert torch.equal(u, v)
+
+
+def test_errors_raise_and_launch_nothing(hc):
+    x = torch.zeros((4, 4, 12), dtype=torch.bfloat16, device="cuda")
+    before = hc.hc_launch_count()
+    with pytest.raises(hc.HcError):
+        hc.hc_pre(x, torch.zeros((4, 4), device="cuda"))    # d % 8 != 0
+    with pytest.raises(hc.HcError):
+        hc.hc_split_sinkhorn(torch.zeros((4, 24), device="cuda"), torch.ones(3, device="cuda"),
+                             torch.zeros(24, device="cuda"), 4, 0)   # iters < 1
+    assert hc.hc_launch_count() == before
