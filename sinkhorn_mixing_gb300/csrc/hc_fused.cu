@@ -24,7 +24,9 @@
 //     from L2) and writes y.
 //   The ring order per CTA is P(0), P(1), C(0), P(2), C(1), ... where P(t)
 //   are the projection boxes of tile t and C(t) its collapse boxes, so the
-//   collapse of a tile overlaps the projection of the next one.
+//   collapse of a tile overlaps the projection of the next one.  Every ring
+//   consumer (MMA thread, square warps, collapse warps) walks every stage in
+//   this order and releases it, using the data only of its own stages.
 //
 // Every wait is bounded: a wait that exceeds kTimeoutNs sets the CTA's abort
 // flag and bit 0 of the device error word, and all roles then run to the
@@ -268,6 +270,13 @@ __host__ __device__ constexpr int bRecvFull(int b) { return 2 * kStages + 8 + b;
 __host__ __device__ constexpr int bRecvFree(int b) { return 2 * kStages + 10 + b; }
 __host__ __device__ constexpr int bPreFull(int b) { return 2 * kStages + 12 + b; }
 constexpr int kMmaDrain = 2 * kStages + 14;
+// Every ring consumer walks every stage in order and releases it once: the
+// MMA thread (1, through tcgen05.commit for P boxes), the 4 square warps and,
+// unless only the mix numbers are wanted, the 4 collapse warps.  Because no
+// consumer skips a stage, each waiter has seen the slot's previous phase and
+// the parity of the phase it waits for is unambiguous.
+constexpr int kEmptyArrivalsFull = 9;
+constexpr int kEmptyArrivalsMixes = 5;
 constexpr int kNumBars = 2 * kStages + 15;
 
 __host__ __device__ constexpr size_t smem_bytes(int nkc) {
@@ -297,15 +306,6 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int nkc) {
     return s;
 }
 
-// Ring sequence numbers of the first box of P(it) and C(it) (see header).
-__device__ __forceinline__ uint32_t seq_p(int it, int nkc, bool mixes_only) {
-    if (mixes_only) return (uint32_t)(it * nkc);
-    return it == 0 ? 0u : (uint32_t)(nkc * (2 * it - 1));
-}
-__device__ __forceinline__ uint32_t seq_c(int it, int T, int nkc) {
-    return (it + 1 < T) ? (uint32_t)(nkc * (2 * it + 2)) : (uint32_t)(nkc * (2 * T - 1));
-}
-
 // Feature index (within the token's F) of K box kc = cc*4 + j of CTA `rank`.
 __device__ __forceinline__ int box_feature(int kc, int rank, const FusedParams &p) {
     const int cc = kc >> 2, j = kc & 3;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(bFull(s)), 1);
-            mbar_init(bar(bEmpty(s)), 4);
+            mbar_init(bar(bEmpty(s)), mixes_only ? kEmptyArrivalsMixes : kEmptyArrivalsFull);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(bAccFull(b)), 1);
@@ -432,78 +432,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wait_bar<false>(bar(bFull(s)), (uint32_t)last_use[s] & 1, abort, p.err);
         }
     } else if (warp == kWarpMma) {
+        // Walks every ring stage in order: P boxes feed the tensor core, C
+        // boxes are only acknowledged (wait for the load, then release).
         if (lane == 0) {
-            for (int it = 0; it < T; ++it) {
-                const int b = it & 1;
-                const uint32_t use = (uint32_t)(it >> 1);
-                if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
-                const uint32_t q0 = seq_p(it, nkc, mixes_only);
-                bool ok = true;
-                for (int kc = 0; kc < nkc; ++kc) {
-                    const uint32_t q = q0 + kc;
-                    const int slot = (int)(q % kStages);
-                    if (!wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err)) {
-                        ok = false;
-                        break;
-                    }
+            uint32_t q = 0;
+            bool ok = true;
+            for (int it = 0; it <= T && ok; ++it) {
+                if (it < T) {
+                    const int b = it & 1;
+                    const uint32_t use = (uint32_t)(it >> 1);
+                    if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
                     tc_fence_after();
-                    const uint32_t a0 = su32(sm.ring + slot * kStageBytes);
-                    const uint32_t b0 = su32(sm.w + (size_t)kc * kWChunkBytes);
+                    const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
+                    for (int kc = 0; kc < nkc; ++kc, ++q) {
+                        const int slot = (int)(q % kStages);
+                        if (!wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = su32(sm.ring + slot * kStageBytes);
+                        const uint32_t b0 = su32(sm.w + (size_t)kc * kWChunkBytes);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
-                                 (kc | k) != 0);
-                    mma_commit(bar(bEmpty(slot)));
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                     (kc | k) != 0);
+                        mma_commit(bar(bEmpty(slot)));
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(bAccFull(b)));
                 }
-                if (!ok) break;
-                mma_commit(bar(bAccFull(b)));
+                if (!mixes_only && it >= 1) {
+                    for (int kc = 0; kc < nkc; ++kc, ++q) {
+                        const int slot = (int)(q % kStages);
+                        if (!wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive(bar(bEmpty(slot)));
+                    }
+                }
             }
             // all issued MMAs complete before TMEM is freed
             mma_commit(bar(kMmaDrain));
             wait_bar<false>(bar(kMmaDrain), 0, abort, p.err);
         }
     } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
-        // sums of squares: warp 2+j handles the boxes of copy j; lane l
-        // accumulates tokens l and l+32 of the tile.
+        // Sums of squares: warp 2+j uses the P boxes of copy j (lane l
+        // accumulates tokens l and l+32 of the tile) and acknowledges every
+        // other stage of the ring.
         const int j = warp - kWarpSq0;
-        for (int it = 0; it < T; ++it) {
-            const int b = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
-            const uint32_t q0 = seq_p(it, nkc, mixes_only);
-            float s0 = 0.f, s1 = 0.f;
-            bool ok = true;
-            for (int cc = 0; cc < p.ncc; ++cc) {
-                const uint32_t q = q0 + cc * 4 + j;
-                const int slot = (int)(q % kStages);
+        uint32_t q = 0;
+        bool ok = true;
+        for (int it = 0; it <= T && ok; ++it) {
+            if (it < T) {
+                const int b = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                float s0 = 0.f, s1 = 0.f;
+                for (int kc = 0; kc < nkc; ++kc, ++q) {
+                    const int slot = (int)(q % kStages);
+                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
+                                                                 (q / kStages) & 1, abort, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    if ((kc & 3) == j) {
+                        const uint32_t base = su32(sm.ring + slot * kStageBytes);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            float f[8];
+                            unpack8(lds128(base + lane * 128 + c * 16), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) s0 = fmaf(f[e], f[e], s0);
+                            unpack8(lds128(base + (lane + 32) * 128 + c * 16), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) s1 = fmaf(f[e], f[e], s1);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
+                }
+                if (!ok) break;
                 if (!__all_sync(0xFFFFFFFFu,
-                                wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err))) {
-                    ok = false;
+                                wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
                     break;
-                }
-                const uint32_t base = su32(sm.ring + slot * kStageBytes);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float f[8];
-                    unpack8(lds128(base + lane * 128 + c * 16), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) s0 = fmaf(f[e], f[e], s0);
-                    unpack8(lds128(base + (lane + 32) * 128 + c * 16), f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) s1 = fmaf(f[e], f[e], s1);
-                }
+                sm.sq[(b * 4 + j) * kTM + lane] = s0;
+                sm.sq[(b * 4 + j) * kTM + lane + 32] = s1;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bEmpty(slot)), 3);
+                if (lane == 0) mbar_arrive(bar(bSqFull(b)));
             }
-            if (!ok) break;
-            if (!__all_sync(0xFFFFFFFFu,
-                            wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
-                break;
-            sm.sq[(b * 4 + j) * kTM + lane] = s0;
-            sm.sq[(b * 4 + j) * kTM + lane + 32] = s1;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bSqFull(b)));
+            if (!mixes_only && it >= 1) {
+                for (int kc = 0; kc < nkc; ++kc, ++q) {
+                    const int slot = (int)(q % kStages);
+                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
+                                                                 (q / kStages) & 1, abort, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
+                }
+            }
         }
     } else if (warp == kWarpEpi0 || warp == kWarpEpi0 + 1) {
         // TMEM lanes 32*(warp%4) .. +31 = tokens of the tile
@@ -608,24 +637,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xFFFFFFFFu, owner_ok)) break;
         }
     } else if (!mixes_only) {
-        // collapse warps 6, 7, 10, 11 -> cw 0..3, 16 tokens each
+        // Collapse warps 6, 7, 10, 11 -> cw 0..3, 16 tokens each.  They
+        // acknowledge the P boxes and use the C boxes, 4 copies at a time.
         const int cw = warp < kWarpEpi0 ? warp - 6 : warp - 8;
         const int w = p.ncc * 64;
-        for (int it = 0; it < T; ++it) {
-            const int b = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
-            const int tile = cluster + it * nclusters;
+        uint32_t q = 0;
+        bool ok = true;
+        for (int it = 0; it <= T && ok; ++it) {
+            if (it < T) {
+                for (int kc = 0; kc < nkc; ++kc, ++q) {
+                    const int slot = (int)(q % kStages);
+                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
+                                                                 (q / kStages) & 1, abort, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
+                }
+                if (!ok) break;
+            }
+            if (it < 1) continue;
+            const int tt = it - 1;
+            const int b = tt & 1;
+            const uint32_t use = (uint32_t)(tt >> 1);
+            const int tile = cluster + tt * nclusters;
             if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(bPreFull(b)), use & 1, abort, p.err)))
                 break;
-            const uint32_t q0 = seq_c(it, T, nkc);
-            bool ok = true;
-            for (int cc = 0; cc < p.ncc && ok; ++cc) {
+            for (int cc = 0; cc < p.ncc && ok; ++cc, q += 4) {
                 int slot[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t q = q0 + cc * 4 + j;
-                    slot[j] = (int)(q % kStages);
-                    if (ok && !wait_bar<false>(bar(bFull(slot[j])), (q / kStages) & 1, abort,
+                    const uint32_t qj = q + j;
+                    slot[j] = (int)(qj % kStages);
+                    if (ok && !wait_bar<false>(bar(bFull(slot[j])), (qj / kStages) & 1, abort,
                                                p.err))
                         ok = false;
                 }
@@ -662,7 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 4; ++j) mbar_arrive(bar(bEmpty(slot[j])));
                 }
             }
-            if (!ok) break;
         }
     }
 
