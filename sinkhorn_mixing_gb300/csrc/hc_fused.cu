@@ -52,7 +52,7 @@ constexpr int kStageBytes = kTM * 128;   // one [64 x 64] bf16 box
 constexpr int kWChunkBytes = kNW * 128;  // one [48 x 64] bf16 chunk of W
 constexpr int kOwn = kTM / kCluster;     // tokens owned per CTA per tile
 constexpr int kRec = 28;                 // floats per partial record (24 + ssq + pad)
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;
 constexpr int kTmemCols = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
@@ -60,7 +60,8 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpSq0 = 2;   // 2..5: sums of squares, warp 2+j takes copy j
-constexpr int kWarpEpi0 = 8;  // 8, 9: TMEM read-out (lanes 0..63), exchange, owners
+constexpr int kWarpEpi0 = 8;  // 8, 9: TMEM read-out (lanes 0..63), records to the owners
+constexpr int kWarpOwner = 12;  // reduces the records of this CTA's tokens, Sinkhorn
 // collapse warps: 6, 7, 10, 11
 
 // tcgen05 instruction descriptor: D f32, A/B bf16, both K-major, N=48, M=128.
@@ -254,6 +255,7 @@ struct Smem {
     float *recv;      // [2][kCluster][kOwn][kRec]   partials received as owner
     float *pre;       // [2][kTM][4]                 pre of the tile's tokens
     float *sq;        // [2][4][kTM]                 partial sums of squares
+    float *stage;     // [kOwn][4]                   pre of the owned tokens
     uint64_t *bar;    // barriers, see below
     uint32_t *tmem;   // TMEM base address written by tcgen05.alloc
     int *abort;
@@ -282,7 +284,7 @@ constexpr int kNumBars = 2 * kStages + 15;
 __host__ __device__ constexpr size_t smem_bytes(int nkc) {
     return 1024 /* alignment slack */ + (size_t)nkc * kWChunkBytes +
            (size_t)kStages * kStageBytes + 2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 * 4 +
-           2 * 4 * kTM * 4 + kNumBars * 8 + 16;
+           2 * 4 * kTM * 4 + kOwn * 4 * 4 + kNumBars * 8 + 16;
 }
 
 __device__ __forceinline__ Smem carve(uint8_t *raw, int nkc) {
@@ -299,6 +301,8 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int nkc) {
     p += 2 * kTM * 4 * 4;
     s.sq = reinterpret_cast<float *>(p);
     p += 2 * 4 * kTM * 4;
+    s.stage = reinterpret_cast<float *>(p);
+    p += kOwn * 4 * 4;
     s.bar = reinterpret_cast<uint64_t *>(p);
     p += kNumBars * 8;
     s.tmem = reinterpret_cast<uint32_t *>(p);
@@ -341,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bSqFull(b)), 4);
             mbar_init(bar(bSqEmpty(b)), 2);
             mbar_init(bar(bRecvFull(b)), kCluster * kOwn);
-            mbar_init(bar(bRecvFree(b)), kCluster * kOwn);
-            mbar_init(bar(bPreFull(b)), kCluster * kOwn);
+            mbar_init(bar(bRecvFree(b)), kCluster);
+            mbar_init(bar(bPreFull(b)), kCluster);
         }
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -501,10 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 8; ++c) {
                             float f[8];
-                            unpack8(lds128(base + lane * 128 + c * 16), f);
+                            // chunk c ^ (row & 7): the same 8 chunks of the row, and
+                            // 8 consecutive lanes touch 8 different bank groups
+                            unpack8(lds128(base + lane * 128 + ((c ^ (lane & 7)) << 4)), f);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) s0 = fmaf(f[e], f[e], s0);
-                            unpack8(lds128(base + (lane + 32) * 128 + c * 16), f);
+                            unpack8(lds128(base + (lane + 32) * 128 + ((c ^ (lane & 7)) << 4)), f);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) s1 = fmaf(f[e], f[e], s1);
                         }
@@ -576,15 +582,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_cluster_v4(rec + 96, ss, 0.f, 0.f, 0.f);
             mbar_arrive_remote(mapa(bar(bRecvFull(b)), (uint32_t)owner));
 
-            // ---- owner: tokens rank*kOwn + lane of this tile
-            bool owner_ok = true;
-            if (warp == kWarpEpi0 && lane < kOwn)
-                owner_ok = wait_bar<true>(bar(bRecvFull(b)), use & 1, abort, p.err);
-            if (warp == kWarpEpi0 && lane < kOwn && owner_ok) {
-                float m[kMix];
+        }
+    } else if (warp == kWarpOwner) {
+        // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: lanes u < kOwn
+        // reduce the 16 records of their token in a fixed order, form r and m,
+        // run split + Sinkhorn; lanes 0..15 then release the record slots and
+        // deliver pre to CTA `lane`, one release-ordered arrive each.
+        float bse[kMix], s0 = 0.f, s1 = 0.f, s2 = 0.f;
+        if (!mixes_only && lane < kOwn) {
+#pragma unroll
+            for (int k = 0; k < kMix; ++k) bse[k] = __ldg(p.base + k);
+            s0 = __ldg(p.scale + 0);
+            s1 = __ldg(p.scale + 1);
+            s2 = __ldg(p.scale + 2);
+        }
+        for (int it = 0; it < T; ++it) {
+            const int b = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            const int tile = cluster + it * nclusters;
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait_bar<true>(bar(bRecvFull(b)), use & 1, abort, p.err)))
+                break;
+            float m[kMix];
+            float ssum = 0.f;
+            if (lane < kOwn) {
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) m[k] = 0.f;
-                float ssum = 0.f;
                 for (int src = 0; src < kCluster; ++src) {
                     const float4 *r4 = reinterpret_cast<const float4 *>(
                         sm.recv + ((b * kCluster + src) * kOwn + lane) * kRec);
@@ -598,9 +621,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ssum += r4[6].x;
                 }
-                // records read: release this slot to every sender
-                for (int dst = 0; dst < kCluster; ++dst)
-                    mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)dst));
+            }
+            __syncwarp();
+            // all records of this parity read: release them to every sender
+            if (lane < kCluster) mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)lane));
+            if (lane < kOwn) {
                 const float r = rsqrtf(ssum / p.F + p.norm_eps);
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) m[k] *= r;
@@ -614,11 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mixes_only) {
                     float pr[4], po[4], Cm[4][4];
                     split_sinkhorn_token<4>([&](int k) { return m[k]; },
-                                            [&](int k) { return __ldg(p.base + k); },
-                                            __ldg(p.scale + 0), __ldg(p.scale + 1),
-                                            __ldg(p.scale + 2), p.iters, p.eps, pr, po, Cm);
+                                            [&](int k) { return bse[k]; }, s0, s1, s2, p.iters,
+                                            p.eps, pr, po, Cm);
                     if (t < p.n) {
-                        reinterpret_cast<float4 *>(p.pre)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+                        reinterpret_cast<float4 *>(p.pre)[t] =
+                            make_float4(pr[0], pr[1], pr[2], pr[3]);
                         reinterpret_cast<float4 *>(p.post)[t] =
                             make_float4(po[0], po[1], po[2], po[3]);
 #pragma unroll
@@ -626,15 +651,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                             reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
                                 make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
                     }
-                    const uint32_t pa = su32(sm.pre + (b * kTM + rank * kOwn + lane) * 4);
-                    for (int dst = 0; dst < kCluster; ++dst) {
-                        st_cluster_v4(mapa(pa, (uint32_t)dst), pr[0], pr[1], pr[2], pr[3]);
-                        mbar_arrive_remote(mapa(bar(bPreFull(b)), (uint32_t)dst));
-                    }
+                    reinterpret_cast<float4 *>(sm.stage)[lane] =
+                        make_float4(pr[0], pr[1], pr[2], pr[3]);
                 }
             }
-            // reconverge (the next tile starts with warp-wide tcgen05.ld)
-            if (!__all_sync(0xFFFFFFFFu, owner_ok)) break;
+            __syncwarp();
+            if (!mixes_only && lane < kCluster) {
+                const uint32_t pa = su32(sm.pre + (b * kTM + rank * kOwn) * 4);
+#pragma unroll
+                for (int u = 0; u < kOwn; ++u) {
+                    const float4 v4 = reinterpret_cast<const float4 *>(sm.stage)[u];
+                    st_cluster_v4(mapa(pa + 16 * u, (uint32_t)lane), v4.x, v4.y, v4.z, v4.w);
+                }
+                mbar_arrive_remote(mapa(bar(bPreFull(b)), (uint32_t)lane));
+            }
+            __syncwarp();
         }
     } else if (!mixes_only) {
         // Collapse warps 6, 7, 10, 11 -> cw 0..3, 16 tokens each.  They
