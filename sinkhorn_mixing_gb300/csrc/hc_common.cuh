@@ -51,32 +51,49 @@ __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, 
 
 // ------------------------------------------------- split + Sinkhorn
 
-__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+// 1/x for finite, positive, normal x: the hardware approximation refined by one
+// Newton-Raphson step for the reciprocal, r' = r + r*(1 - x*r), which brings it
+// to about 1 ulp.  (The correctly rounded division is a long subroutine; on the
+// per-token critical path of the fused kernel it cost ~25x more.)
+__device__ __forceinline__ float rcp_refined(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return fmaf(r, fmaf(-x, r, 1.0f), r);
+}
 
-// One token.  m: the token's (2+HC)*HC mix numbers; s0..s2 = hc_scale;
-// base = hc_base.  Outputs pre[HC], post[HC], C[HC][HC] (row j, column k).
+// sigmoid(z) = 1 / (1 + e^-z), with the exponential of -|z| only (never
+// overflows): sigmoid(z) = 1/(1+e) for z >= 0 and e/(1+e) for z < 0, e = e^-|z|.
+__device__ __forceinline__ float sigmoidf_(float z) {
+    const float e = expf(-fabsf(z));
+    const float r = rcp_refined(1.0f + e);
+    return z >= 0.f ? r : e * r;
+}
+
+// pre and post of one token ("Reading weights" page, pre formula and the
+// hc_split_sinkhorn kernel):
 //   pre_j  = sigmoid(m_j s0 + b_j) + eps
 //   post_j = 2 sigmoid(m_{HC+j} s1 + b_{HC+j})
-//   L_jk   = m_{2HC+j HC+k} s2 + b_{2HC+j HC+k}
-//   C = rowsoftmax(L) + eps; column step; (iters-1) x (row step, column step)
-// A step divides by (sum + eps); the division is done as a multiplication by
-// the correctly rounded reciprocal of the shared denominator.
 template <int HC, typename MixFn, typename BaseFn>
-__device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float s0, float s1,
-                                                     float s2, int iters, float eps,
-                                                     float pre[HC], float post[HC],
-                                                     float C[HC][HC]) {
+__device__ __forceinline__ void split_pre_post(MixFn m, BaseFn base, float s0, float s1, float eps,
+                                               float pre[HC], float post[HC]) {
 #pragma unroll
     for (int j = 0; j < HC; ++j) pre[j] = sigmoidf_(fmaf(m(j), s0, base(j))) + eps;
 #pragma unroll
     for (int j = 0; j < HC; ++j) post[j] = 2.0f * sigmoidf_(fmaf(m(HC + j), s1, base(HC + j)));
+}
+
+// comb of one token (same kernel on the same page): with
+//   L_jk = m_{2HC+j HC+k} s2 + b_{2HC+j HC+k}   (row j, column k)
+// C = row softmax of L (max-subtracted, plain row sum) + eps; a column step;
+// then (iters-1) x (row step, column step), each step dividing by (sum + eps).
+template <int HC, typename MixFn, typename BaseFn>
+__device__ __forceinline__ void sinkhorn_comb(MixFn m, BaseFn base, float s2, int iters, float eps,
+                                              float C[HC][HC]) {
 #pragma unroll
     for (int j = 0; j < HC; ++j)
 #pragma unroll
         for (int k = 0; k < HC; ++k)
             C[j][k] = fmaf(m(2 * HC + j * HC + k), s2, base(2 * HC + j * HC + k));
-
-    // row softmax (max-subtracted, plain row sum), then + eps
 #pragma unroll
     for (int j = 0; j < HC; ++j) {
         float mx = C[j][0];
@@ -88,7 +105,7 @@ __device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float
             C[j][k] = expf(C[j][k] - mx);
             s += C[j][k];
         }
-        const float inv = 1.0f / s;
+        const float inv = rcp_refined(s);  // s >= 1: the row maximum contributes e^0
 #pragma unroll
         for (int k = 0; k < HC; ++k) C[j][k] = fmaf(C[j][k], inv, eps);
     }
@@ -98,7 +115,7 @@ __device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float
         float s = 0.0f;
 #pragma unroll
         for (int j = 0; j < HC; ++j) s += C[j][k];
-        const float inv = 1.0f / (s + eps);
+        const float inv = rcp_refined(s + eps);
 #pragma unroll
         for (int j = 0; j < HC; ++j) C[j][k] *= inv;
     }
@@ -108,7 +125,7 @@ __device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float
             float s = 0.0f;
 #pragma unroll
             for (int k = 0; k < HC; ++k) s += C[j][k];
-            const float inv = 1.0f / (s + eps);
+            const float inv = rcp_refined(s + eps);
 #pragma unroll
             for (int k = 0; k < HC; ++k) C[j][k] *= inv;
         }
@@ -117,11 +134,21 @@ __device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float
             float s = 0.0f;
 #pragma unroll
             for (int j = 0; j < HC; ++j) s += C[j][k];
-            const float inv = 1.0f / (s + eps);
+            const float inv = rcp_refined(s + eps);
 #pragma unroll
             for (int j = 0; j < HC; ++j) C[j][k] *= inv;
         }
     }
+}
+
+// One token: m = its (2+HC)*HC mix numbers, s0..s2 = hc_scale, base = hc_base.
+template <int HC, typename MixFn, typename BaseFn>
+__device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float s0, float s1,
+                                                     float s2, int iters, float eps,
+                                                     float pre[HC], float post[HC],
+                                                     float C[HC][HC]) {
+    split_pre_post<HC>(m, base, s0, s1, eps, pre, post);
+    sinkhorn_comb<HC>(m, base, s2, iters, eps, C);
 }
 
 }  // namespace hc

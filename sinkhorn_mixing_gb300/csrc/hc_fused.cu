@@ -9,24 +9,25 @@
 //   * The CTA keeps its slice of W_mix resident in shared memory for the whole
 //     kernel, split into bf16 hi + lo rows (48 rows = 24 hi, 24 lo), in the
 //     128-byte-swizzled K-major layout the tensor core reads.
-//   * x streams through an 8-stage ring of [64 tokens x 64 features] TMA
-//     boxes.  Per box: 4 tcgen05.mma (M=128 rows of which the 64 tokens are
-//     the first half, N=48, K=16) accumulate x.(W_hi + W_lo) in TMEM
-//     (binary32), and one of 4 "square" warps adds the box's x^2 per token.
+//   * x streams through a 2-slot ring: one TMA operation per (tile, copy)
+//     brings the copy's w channels of the tile's 64 tokens (w/64 swizzled
+//     [64 x 64] sub-tiles, 40 KB at d = 5120).  Few, large TMA operations
+//     matter: the per-CTA rate of TMA operations, not their size, bounds the
+//     bandwidth of small boxes.  Per sub-tile, 4 tcgen05.mma (M=128 rows of
+//     which the 64 tokens are the first half, N=48, K=16) accumulate
+//     x.(W_hi + W_lo) in TMEM (binary32); 4 square warps add x^2 per token.
 //   * At the end of a tile each CTA sends its 24 partial mix numbers and
 //     partial sum of squares per token to the token's owner CTA (4 tokens per
-//     CTA) through distributed shared memory.  The owner reduces the 16
-//     partials in a fixed order, forms r and m, runs the split + Sinkhorn for
-//     its tokens, writes pre/post/comb (and m), and broadcasts pre back to
-//     all 16 CTAs.
-//   * The collapse y = sum_j pre_j x_j re-reads the tile's x slice through
-//     the same ring (the boxes were read a few microseconds earlier and come
-//     from L2) and writes y.
-//   The ring order per CTA is P(0), P(1), C(0), P(2), C(1), ... where P(t)
-//   are the projection boxes of tile t and C(t) its collapse boxes, so the
-//   collapse of a tile overlaps the projection of the next one.  Every ring
-//   consumer (MMA thread, square warps, collapse warps) walks every stage in
-//   this order and releases it, using the data only of its own stages.
+//     CTA) through distributed shared memory.  The owner warp reduces the 16
+//     records in a fixed order, forms r and m, runs the split + Sinkhorn,
+//     writes pre/post/comb (and m) and broadcasts pre to all 16 CTAs.
+//   * The collapse y = sum_j pre_j x_j re-reads the tile's x slice with
+//     16-byte loads (the bytes were fetched from HBM by the TMA a few
+//     microseconds earlier and are served by L2) and writes y; when done it
+//     releases its pre buffer to every owner.
+//   Every consumer of the ring (MMA thread, 4 square warps) waits on and
+//   releases every stage in order, so each wait is for the phase right after
+//   one it has already seen.
 //
 // Every wait is bounded: a wait that exceeds kTimeoutNs sets the CTA's abort
 // flag and bit 0 of the device error word, and all roles then run to the
@@ -43,26 +44,32 @@
 namespace hc {
 namespace {
 
-constexpr int kCluster = 16;        // CTAs per cluster
-constexpr int kTM = 64;             // tokens per tile
-constexpr int kMix = 24;            // (2 + 4) * 4
-constexpr int kNW = 48;             // B rows: 24 hi + 24 lo
-constexpr int kStages = 8;          // x ring depth
-constexpr int kStageBytes = kTM * 128;   // one [64 x 64] bf16 box
+constexpr int kCluster = 16;             // CTAs per cluster
+constexpr int kTM = 64;                  // tokens per tile
+constexpr int kMix = 24;                 // (2 + 4) * 4
+constexpr int kNW = 48;                  // B rows: 24 hi + 24 lo
+constexpr int kSlots = 2;                // x ring depth (one copy of a tile per slot)
+constexpr int kSubBytes = kTM * 128;     // one swizzled [64 tokens x 64 channels] sub-tile
 constexpr int kWChunkBytes = kNW * 128;  // one [48 x 64] bf16 chunk of W
 constexpr int kOwn = kTM / kCluster;     // tokens owned per CTA per tile
 constexpr int kRec = 28;                 // floats per partial record (24 + ssq + pad)
-constexpr int kThreads = 416;
+constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 
-// warp roles
+// warp roles (16 warps: 512 threads leave 128 registers per thread)
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
-constexpr int kWarpSq0 = 2;   // 2..5: sums of squares, warp 2+j takes copy j
-constexpr int kWarpEpi0 = 8;  // 8, 9: TMEM read-out (lanes 0..63), records to the owners
-constexpr int kWarpOwner = 12;  // reduces the records of this CTA's tokens, Sinkhorn
-// collapse warps: 6, 7, 10, 11
+constexpr int kWarpSq0 = 2;      // 2..5: sums of squares, 16 tokens each
+constexpr int kWarpEpi0 = 8;     // 8, 9: TMEM read-out (lanes 0..63), records to owners
+constexpr int kWarpOwner = 12;   // reduces the records of this CTA's tokens, Sinkhorn
+constexpr int kCollapseWarps = 7;  // 6, 7, 10, 11, 13, 14, 15
+constexpr int kThreads = 16 * 32;
+constexpr int kCollapseThreads = kCollapseWarps * 32;
+
+__host__ __device__ constexpr int collapse_index(int warp) {
+    return warp == 6 ? 0 : warp == 7 ? 1 : warp == 10 ? 2 : warp == 11 ? 3 : warp - 9;
+}
 
 // tcgen05 instruction descriptor: D f32, A/B bf16, both K-major, N=48, M=128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNW >> 3) << 17) |
@@ -71,14 +78,14 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNW
 struct FusedParams {
     int64_t n;
     int d;
-    int ncc;        // 64-channel chunks per CTA slice (w / 64)
-    int nkc;        // K boxes per CTA per tile (4 * ncc)
+    int ncc;        // 64-channel sub-tiles per copy per CTA (w / 64)
     int num_tiles;
     int iters;
     int mixes_only;
     float eps;
     float norm_eps;
     float F;
+    const uint16_t *x;
     const float *w;
     const float *scale;
     const float *base;
@@ -183,12 +190,12 @@ __device__ __forceinline__ void cluster_sync_all() {
                      : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
 
@@ -250,11 +257,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // ---------------------------------------------------------------- layout
 
 struct Smem {
-    uint8_t *w;       // nkc chunks of [48 x 64] bf16, swizzled
-    uint8_t *ring;    // kStages boxes of [64 x 64] bf16, swizzled
+    uint8_t *w;       // 4*ncc chunks of [48 x 64] bf16, swizzled, chunk = copy*ncc + cc
+    uint8_t *ring;    // kSlots stages of ncc sub-tiles [64 x 64] bf16, swizzled
     float *recv;      // [2][kCluster][kOwn][kRec]   partials received as owner
     float *pre;       // [2][kTM][4]                 pre of the tile's tokens
-    float *sq;        // [2][4][kTM]                 partial sums of squares
+    float *sq;        // [2][kTM]                    this CTA's partial sums of squares
     float *stage;     // [kOwn][4]                   pre of the owned tokens
     uint64_t *bar;    // barriers, see below
     uint32_t *tmem;   // TMEM base address written by tcgen05.alloc
@@ -263,44 +270,45 @@ struct Smem {
 
 // barrier indices
 __host__ __device__ constexpr int bFull(int s) { return s; }
-__host__ __device__ constexpr int bEmpty(int s) { return kStages + s; }
-__host__ __device__ constexpr int bAccFull(int b) { return 2 * kStages + b; }
-__host__ __device__ constexpr int bAccEmpty(int b) { return 2 * kStages + 2 + b; }
-__host__ __device__ constexpr int bSqFull(int b) { return 2 * kStages + 4 + b; }
-__host__ __device__ constexpr int bSqEmpty(int b) { return 2 * kStages + 6 + b; }
-__host__ __device__ constexpr int bRecvFull(int b) { return 2 * kStages + 8 + b; }
-__host__ __device__ constexpr int bRecvFree(int b) { return 2 * kStages + 10 + b; }
-__host__ __device__ constexpr int bPreFull(int b) { return 2 * kStages + 12 + b; }
-constexpr int kMmaDrain = 2 * kStages + 14;
-// Every ring consumer walks every stage in order and releases it once: the
-// MMA thread (1, through tcgen05.commit for P boxes), the 4 square warps and,
-// unless only the mix numbers are wanted, the 4 collapse warps.  Because no
-// consumer skips a stage, each waiter has seen the slot's previous phase and
-// the parity of the phase it waits for is unambiguous.
-constexpr int kEmptyArrivalsFull = 9;
-constexpr int kEmptyArrivalsMixes = 5;
-constexpr int kNumBars = 2 * kStages + 15;
+__host__ __device__ constexpr int bEmpty(int s) { return kSlots + s; }
+__host__ __device__ constexpr int bAccFull(int b) { return 2 * kSlots + b; }
+__host__ __device__ constexpr int bAccEmpty(int b) { return 2 * kSlots + 2 + b; }
+__host__ __device__ constexpr int bSqFull(int b) { return 2 * kSlots + 4 + b; }
+__host__ __device__ constexpr int bSqEmpty(int b) { return 2 * kSlots + 6 + b; }
+__host__ __device__ constexpr int bRecvFull(int b) { return 2 * kSlots + 8 + b; }
+__host__ __device__ constexpr int bRecvFree(int b) { return 2 * kSlots + 10 + b; }
+__host__ __device__ constexpr int bPreFull(int b) { return 2 * kSlots + 12 + b; }
+__host__ __device__ constexpr int bPreFree(int b) { return 2 * kSlots + 14 + b; }
+__host__ __device__ constexpr int bColDone(int b) { return 2 * kSlots + 16 + b; }
+constexpr int kMmaDrain = 2 * kSlots + 18;
+constexpr int kNumBars = 2 * kSlots + 19;
+// Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
+constexpr int kEmptyArrivals = 5;
 
-__host__ __device__ constexpr size_t smem_bytes(int nkc) {
-    return 1024 /* alignment slack */ + (size_t)nkc * kWChunkBytes +
-           (size_t)kStages * kStageBytes + 2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 * 4 +
-           2 * 4 * kTM * 4 + kOwn * 4 * 4 + kNumBars * 8 + 16;
+__host__ __device__ constexpr size_t ring_bytes(int ncc) { return (size_t)kSlots * ncc * kSubBytes; }
+
+__host__ __device__ constexpr size_t smem_bytes(int ncc) {
+    return 1024 /* alignment slack */ + (size_t)4 * ncc * kWChunkBytes + ring_bytes(ncc) +
+           2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 * 4 + 2 * kTM * 4 + kOwn * 4 * 4 +
+           kNumBars * 8 + 16;
 }
 
-__device__ __forceinline__ Smem carve(uint8_t *raw, int nkc) {
+__device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
     uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023;
     uint8_t *p = reinterpret_cast<uint8_t *>(a);
     Smem s;
     s.w = p;
-    p += (size_t)nkc * kWChunkBytes;
+    p += (size_t)4 * ncc * kWChunkBytes;
     s.ring = p;
-    p += kStages * kStageBytes;
+    p += ring_bytes(ncc);
+    // The M=128 operand of the last sub-tile reads 8 KB past the ring (rows
+    // 64..127, never used): the records that follow are at least that large.
     s.recv = reinterpret_cast<float *>(p);
     p += 2 * kCluster * kOwn * kRec * 4;
     s.pre = reinterpret_cast<float *>(p);
     p += 2 * kTM * 4 * 4;
     s.sq = reinterpret_cast<float *>(p);
-    p += 2 * 4 * kTM * 4;
+    p += 2 * kTM * 4;
     s.stage = reinterpret_cast<float *>(p);
     p += kOwn * 4 * 4;
     s.bar = reinterpret_cast<uint64_t *>(p);
@@ -309,10 +317,11 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int nkc) {
     s.abort = reinterpret_cast<int *>(p + 4);
     return s;
 }
+static_assert(2 * kCluster * kOwn * kRec * 4 >= kSubBytes, "overrun of the last sub-tile");
 
-// Feature index (within the token's F) of K box kc = cc*4 + j of CTA `rank`.
-__device__ __forceinline__ int box_feature(int kc, int rank, const FusedParams &p) {
-    const int cc = kc >> 2, j = kc & 3;
+// First feature (within the token's F) of W chunk kc = copy*ncc + cc of CTA `rank`.
+__device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams &p) {
+    const int j = kc / p.ncc, cc = kc % p.ncc;
     return j * p.d + rank * (p.ncc * 64) + cc * 64;
 }
 
@@ -321,12 +330,14 @@ __device__ __forceinline__ int box_feature(int kc, int rank, const FusedParams &
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap tmap, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const Smem sm = carve(smem_raw, p.nkc);
+    const int ncc = p.ncc;
+    const Smem sm = carve(smem_raw, ncc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
     const int cluster = (int)(blockIdx.x / kCluster);
     const int nclusters = (int)(gridDim.x / kCluster);
-    const int nkc = p.nkc;
+    const int w = ncc * 64;
+    const uint32_t stage_bytes = (uint32_t)ncc * kSubBytes;
     const bool mixes_only = p.mixes_only != 0;
     const int T = cluster < p.num_tiles ? (p.num_tiles - cluster + nclusters - 1) / nclusters : 0;
     volatile int *abort = sm.abort;
@@ -335,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
         *abort = 0;
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(bFull(s)), 1);
-            mbar_init(bar(bEmpty(s)), mixes_only ? kEmptyArrivalsMixes : kEmptyArrivalsFull);
+            mbar_init(bar(bEmpty(s)), kEmptyArrivals);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(bAccFull(b)), 1);
@@ -347,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bRecvFull(b)), kCluster * kOwn);
             mbar_init(bar(bRecvFree(b)), kCluster);
             mbar_init(bar(bPreFull(b)), kCluster);
+            mbar_init(bar(bPreFree(b)), kCluster);
+            mbar_init(bar(bColDone(b)), kCollapseWarps);
         }
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -364,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // W slice -> bf16 hi/lo rows in the swizzled K-major layout.  Row nr < 24
     // holds hi(W[nr]), row 24 + i holds lo(W[i]) = bf16(W - hi).
     {
+        const int nkc = 4 * ncc;
         const int total = kNW * nkc * 8;
         const int64_t F = 4LL * p.d;
         for (int idx = threadIdx.x; idx < total; idx += kThreads) {
@@ -372,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int i = nr % kMix;
             const bool lo = nr >= kMix;
             const float4 *src = reinterpret_cast<const float4 *>(
-                p.w + (int64_t)i * F + box_feature(kc, rank, p) + q * 8);
+                p.w + (int64_t)i * F + chunk_feature(kc, rank, p) + q * 8);
             const float4 a = __ldg(src), b2 = __ldg(src + 1);
             float v[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
             if (lo) {
@@ -399,146 +413,106 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ roles
     if (warp == kWarpProducer) {
+        // stage q = 4*it + copy: the copy's w channels of the tile's 64 tokens
         if (lane == 0) {
-            uint32_t q = 0;
-            int last_use[kStages];
-#pragma unroll
-            for (int s = 0; s < kStages; ++s) last_use[s] = -1;
+            int last_use[kSlots] = {-1, -1};
             bool ok = true;
-            for (int it = 0; it <= T && ok; ++it) {
-                for (int part = 0; part < 2 && ok; ++part) {
-                    int tt;
-                    if (part == 0) {
-                        if (it >= T) continue;
-                        tt = it;
-                    } else {
-                        if (mixes_only || it < 1) continue;
-                        tt = it - 1;
+            for (int it = 0; it < T && ok; ++it) {
+                const int tile = cluster + it * nclusters;
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t q = (uint32_t)(4 * it + j);
+                    const int slot = (int)(q % kSlots);
+                    const uint32_t use = q / kSlots;
+                    if (!wait_bar<false>(bar(bEmpty(slot)), (use & 1) ^ 1, abort, p.err)) {
+                        ok = false;
+                        break;
                     }
-                    const int tile = cluster + tt * nclusters;
-                    for (int kc = 0; kc < nkc; ++kc, ++q) {
-                        const int slot = (int)(q % kStages);
-                        const uint32_t use = q / kStages;
-                        if (!wait_bar<false>(bar(bEmpty(slot)), (use & 1) ^ 1, abort, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_expect_tx(bar(bFull(slot)), kStageBytes);
-                        tma_load_2d(su32(sm.ring + slot * kStageBytes), &tmap,
-                                    box_feature(kc, rank, p), tile * kTM, bar(bFull(slot)));
-                        last_use[slot] = (int)use;
-                    }
+                    mbar_expect_tx(bar(bFull(slot)), stage_bytes);
+                    tma_load_3d(su32(sm.ring + slot * stage_bytes), &tmap, 0, tile * kTM,
+                                (j * p.d + rank * w) / 64, bar(bFull(slot)));
+                    last_use[slot] = (int)use;
                 }
             }
             // no TMA may still be writing this CTA's shared memory at exit
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < kSlots; ++s)
                 if (last_use[s] >= 0)
                     wait_bar<false>(bar(bFull(s)), (uint32_t)last_use[s] & 1, abort, p.err);
         }
     } else if (warp == kWarpMma) {
-        // Walks every ring stage in order: P boxes feed the tensor core, C
-        // boxes are only acknowledged (wait for the load, then release).
         if (lane == 0) {
-            uint32_t q = 0;
             bool ok = true;
-            for (int it = 0; it <= T && ok; ++it) {
-                if (it < T) {
-                    const int b = it & 1;
-                    const uint32_t use = (uint32_t)(it >> 1);
-                    if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
+            for (int it = 0; it < T && ok; ++it) {
+                const int b = it & 1;
+                const uint32_t use = (uint32_t)(it >> 1);
+                if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t q = (uint32_t)(4 * it + j);
+                    const int slot = (int)(q % kSlots);
+                    if (!wait_bar<false>(bar(bFull(slot)), (q / kSlots) & 1, abort, p.err)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
-                    for (int kc = 0; kc < nkc; ++kc, ++q) {
-                        const int slot = (int)(q % kStages);
-                        if (!wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a0 = su32(sm.ring + slot * kStageBytes);
-                        const uint32_t b0 = su32(sm.w + (size_t)kc * kWChunkBytes);
+                    const uint32_t a0 = su32(sm.ring + slot * stage_bytes);
+                    const uint32_t b0 = su32(sm.w + (size_t)(j * ncc) * kWChunkBytes);
+                    for (int cc = 0; cc < ncc; ++cc) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
-                                     (kc | k) != 0);
-                        mma_commit(bar(bEmpty(slot)));
+                            mma_bf16(d_tmem, sw128_desc(a0 + cc * kSubBytes + 32 * k),
+                                     sw128_desc(b0 + cc * kWChunkBytes + 32 * k),
+                                     (j | cc | k) != 0);
                     }
-                    if (!ok) break;
-                    mma_commit(bar(bAccFull(b)));
+                    mma_commit(bar(bEmpty(slot)));
                 }
-                if (!mixes_only && it >= 1) {
-                    for (int kc = 0; kc < nkc; ++kc, ++q) {
-                        const int slot = (int)(q % kStages);
-                        if (!wait_bar<false>(bar(bFull(slot)), (q / kStages) & 1, abort, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive(bar(bEmpty(slot)));
-                    }
-                }
+                if (!ok) break;
+                mma_commit(bar(bAccFull(b)));
             }
             // all issued MMAs complete before TMEM is freed
             mma_commit(bar(kMmaDrain));
             wait_bar<false>(bar(kMmaDrain), 0, abort, p.err);
         }
     } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
-        // Sums of squares: warp 2+j uses the P boxes of copy j (lane l
-        // accumulates tokens l and l+32 of the tile) and acknowledges every
-        // other stage of the ring.
-        const int j = warp - kWarpSq0;
-        uint32_t q = 0;
+        // Sums of squares: warp 2+g covers tokens 16g..16g+15 of every stage;
+        // lane -> token 16g + lane/2, half lane%2 of each 128-byte row.
+        const int i = 16 * (warp - kWarpSq0) + (lane >> 1);
+        const int h = lane & 1;
         bool ok = true;
-        for (int it = 0; it <= T && ok; ++it) {
-            if (it < T) {
-                const int b = it & 1;
-                const uint32_t use = (uint32_t)(it >> 1);
-                float s0 = 0.f, s1 = 0.f;
-                for (int kc = 0; kc < nkc; ++kc, ++q) {
-                    const int slot = (int)(q % kStages);
-                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
-                                                                 (q / kStages) & 1, abort, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    if ((kc & 3) == j) {
-                        const uint32_t base = su32(sm.ring + slot * kStageBytes);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            float f[8];
-                            // chunk c ^ (row & 7): the same 8 chunks of the row, and
-                            // 8 consecutive lanes touch 8 different bank groups
-                            unpack8(lds128(base + lane * 128 + ((c ^ (lane & 7)) << 4)), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) s0 = fmaf(f[e], f[e], s0);
-                            unpack8(lds128(base + (lane + 32) * 128 + ((c ^ (lane & 7)) << 4)), f);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) s1 = fmaf(f[e], f[e], s1);
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
-                }
-                if (!ok) break;
-                if (!__all_sync(0xFFFFFFFFu,
-                                wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
+        for (int it = 0; it < T && ok; ++it) {
+            const int b = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            float ss = 0.f;
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t q = (uint32_t)(4 * it + j);
+                const int slot = (int)(q % kSlots);
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)), (q / kSlots) & 1,
+                                                             abort, p.err))) {
+                    ok = false;
                     break;
-                sm.sq[(b * 4 + j) * kTM + lane] = s0;
-                sm.sq[(b * 4 + j) * kTM + lane + 32] = s1;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bSqFull(b)));
-            }
-            if (!mixes_only && it >= 1) {
-                for (int kc = 0; kc < nkc; ++kc, ++q) {
-                    const int slot = (int)(q % kStages);
-                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
-                                                                 (q / kStages) & 1, abort, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
                 }
+                const uint32_t base = su32(sm.ring + slot * stage_bytes) + i * 128;
+                for (int cc = 0; cc < ncc; ++cc) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        // chunk (4h+m) ^ (row & 7): 8 consecutive lanes hit 8 bank groups
+                        float f[8];
+                        unpack8(lds128(base + cc * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4)), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
             }
+            if (!ok) break;
+            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
+                break;
+            if (h == 0) sm.sq[b * kTM + i] = ss;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bSqFull(b)));
         }
     } else if (warp == kWarpEpi0 || warp == kWarpEpi0 + 1) {
         // TMEM lanes 32*(warp%4) .. +31 = tokens of the tile
@@ -547,7 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < T; ++it) {
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            const int tile = cluster + it * nclusters;
             if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bAccFull(b)), use & 1, abort, p.err)))
                 break;
             tc_fence_after();
@@ -562,9 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar(bAccEmpty(b)));
             if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bSqFull(b)), use & 1, abort, p.err)))
                 break;
-            float ss = 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) ss += sm.sq[(b * 4 + jj) * kTM + i];
+            const float ss = sm.sq[b * kTM + i];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bSqEmpty(b)));
             // the owner's record slot for this tile parity must be free
@@ -581,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                               acc[4 * v + 3] + acc[24 + 4 * v + 3]);
             st_cluster_v4(rec + 96, ss, 0.f, 0.f, 0.f);
             mbar_arrive_remote(mapa(bar(bRecvFull(b)), (uint32_t)owner));
-
         }
     } else if (warp == kWarpOwner) {
         // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: lanes u < kOwn
@@ -625,11 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // all records of this parity read: release them to every sender
             if (lane < kCluster) mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)lane));
+            float pr[4], po[4];
+            int64_t t = 0;
             if (lane < kOwn) {
                 const float r = rsqrtf(ssum / p.F + p.norm_eps);
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) m[k] *= r;
-                const int64_t t = (int64_t)tile * kTM + rank * kOwn + lane;
+                t = (int64_t)tile * kTM + rank * kOwn + lane;
                 if (t < p.n && p.mixes != nullptr) {
                     float4 *dst = reinterpret_cast<float4 *>(p.mixes + t * kMix);
 #pragma unroll
@@ -637,10 +609,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[v] = make_float4(m[4 * v], m[4 * v + 1], m[4 * v + 2], m[4 * v + 3]);
                 }
                 if (!mixes_only) {
-                    float pr[4], po[4], Cm[4][4];
-                    split_sinkhorn_token<4>([&](int k) { return m[k]; },
-                                            [&](int k) { return bse[k]; }, s0, s1, s2, p.iters,
-                                            p.eps, pr, po, Cm);
+                    split_pre_post<4>([&](int k) { return m[k]; }, [&](int k) { return bse[k]; },
+                                      s0, s1, p.eps, pr, po);
+                    reinterpret_cast<float4 *>(sm.stage)[lane] =
+                        make_float4(pr[0], pr[1], pr[2], pr[3]);
+                }
+            }
+            __syncwarp();
+            if (!mixes_only) {
+                // pre first (the collapse waits for it); every CTA must have
+                // finished reading this parity's pre buffer
+                bool okf = true;
+                if (lane < kCluster)
+                    okf = wait_bar<true>(bar(bPreFree(b)), (use & 1) ^ 1, abort, p.err);
+                if (!__all_sync(0xFFFFFFFFu, okf)) break;
+                if (lane < kCluster) {
+                    const uint32_t pa = su32(sm.pre + (b * kTM + rank * kOwn) * 4);
+#pragma unroll
+                    for (int uu = 0; uu < kOwn; ++uu) {
+                        const float4 v4 = reinterpret_cast<const float4 *>(sm.stage)[uu];
+                        st_cluster_v4(mapa(pa + 16 * uu, (uint32_t)lane), v4.x, v4.y, v4.z, v4.w);
+                    }
+                    mbar_arrive_remote(mapa(bar(bPreFull(b)), (uint32_t)lane));
+                }
+                // then the Sinkhorn for comb, off the collapse's critical path
+                if (lane < kOwn) {
+                    float Cm[4][4];
+                    sinkhorn_comb<4>([&](int k) { return m[k]; }, [&](int k) { return bse[k]; },
+                                     s2, p.iters, p.eps, Cm);
                     if (t < p.n) {
                         reinterpret_cast<float4 *>(p.pre)[t] =
                             make_float4(pr[0], pr[1], pr[2], pr[3]);
@@ -651,92 +647,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                             reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
                                 make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
                     }
-                    reinterpret_cast<float4 *>(sm.stage)[lane] =
-                        make_float4(pr[0], pr[1], pr[2], pr[3]);
                 }
-            }
-            __syncwarp();
-            if (!mixes_only && lane < kCluster) {
-                const uint32_t pa = su32(sm.pre + (b * kTM + rank * kOwn) * 4);
-#pragma unroll
-                for (int u = 0; u < kOwn; ++u) {
-                    const float4 v4 = reinterpret_cast<const float4 *>(sm.stage)[u];
-                    st_cluster_v4(mapa(pa + 16 * u, (uint32_t)lane), v4.x, v4.y, v4.z, v4.w);
-                }
-                mbar_arrive_remote(mapa(bar(bPreFull(b)), (uint32_t)lane));
             }
             __syncwarp();
         }
     } else if (!mixes_only) {
-        // Collapse warps 6, 7, 10, 11 -> cw 0..3, 16 tokens each.  They
-        // acknowledge the P boxes and use the C boxes, 4 copies at a time.
-        const int cw = warp < kWarpEpi0 ? warp - 6 : warp - 8;
-        const int w = p.ncc * 64;
-        uint32_t q = 0;
-        bool ok = true;
-        for (int it = 0; it <= T && ok; ++it) {
-            if (it < T) {
-                for (int kc = 0; kc < nkc; ++kc, ++q) {
-                    const int slot = (int)(q % kStages);
-                    if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)),
-                                                                 (q / kStages) & 1, abort, p.err))) {
-                        ok = false;
-                        break;
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
-                }
-                if (!ok) break;
-            }
-            if (it < 1) continue;
-            const int tt = it - 1;
-            const int b = tt & 1;
-            const uint32_t use = (uint32_t)(tt >> 1);
-            const int tile = cluster + tt * nclusters;
+        // Collapse: 7 warps, 224 threads.  Output vector o = (token o / (w/8),
+        // 8 channels at 8*(o % (w/8))) of this CTA's slice; 4 vectors in flight
+        // per thread, each needing the 4 copies (16-byte loads from L2).
+        const int ct = collapse_index(warp) * 32 + lane;
+        const int vpt = w / 8;  // vectors per token
+        const int nout = kTM * vpt;
+        const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
+        const int64_t nv = p.d / 8;  // vectors per copy row
+        for (int it = 0; it < T; ++it) {
+            const int b = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            const int tile = cluster + it * nclusters;
             if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(bPreFull(b)), use & 1, abort, p.err)))
                 break;
-            for (int cc = 0; cc < p.ncc && ok; ++cc, q += 4) {
-                int slot[4];
+            constexpr int G = 4;
+            for (int o0 = ct; o0 < nout; o0 += G * kCollapseThreads) {
+                uint4 xv[G][4];
+                int64_t tok[G];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t qj = q + j;
-                    slot[j] = (int)(qj % kStages);
-                    if (ok && !wait_bar<false>(bar(bFull(slot[j])), (qj / kStages) & 1, abort,
-                                               p.err))
-                        ok = false;
+                for (int g = 0; g < G; ++g) {
+                    const int o = o0 + g * kCollapseThreads;
+                    tok[g] = (int64_t)tile * kTM + o / vpt;
+                    if (o < nout && tok[g] < p.n) {
+                        const int64_t v = (int64_t)rank * vpt + o % vpt;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) xv[g][j] = __ldcs(x + (tok[g] * 4 + j) * nv + v);
+                    }
                 }
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
 #pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const int i = 16 * cw + 4 * uu + (lane >> 3);
-                    const int mch = lane & 7;
-                    const float4 pr = *reinterpret_cast<const float4 *>(sm.pre + (b * kTM + i) * 4);
-                    const uint32_t off = i * 128 + ((mch ^ (i & 7)) << 4);
-                    float acc[8], f[8];
-                    unpack8(lds128(su32(sm.ring + slot[0] * kStageBytes) + off), f);
+                for (int g = 0; g < G; ++g) {
+                    const int o = o0 + g * kCollapseThreads;
+                    if (o < nout && tok[g] < p.n) {
+                        const float4 pr =
+                            *reinterpret_cast<const float4 *>(sm.pre + (b * kTM + o / vpt) * 4);
+                        float acc[8], f[8];
+                        unpack8(xv[g][0], f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
-                    unpack8(lds128(su32(sm.ring + slot[1] * kStageBytes) + off), f);
+                        for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
+                        unpack8(xv[g][1], f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
-                    unpack8(lds128(su32(sm.ring + slot[2] * kStageBytes) + off), f);
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
+                        unpack8(xv[g][2], f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
-                    unpack8(lds128(su32(sm.ring + slot[3] * kStageBytes) + off), f);
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
+                        unpack8(xv[g][3], f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
-                    const int64_t t = (int64_t)tile * kTM + i;
-                    if (t < p.n)
-                        st_stream(reinterpret_cast<uint4 *>(p.y + t * p.d + rank * w + cc * 64 +
-                                                            mch * 8),
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
+                        st_stream(reinterpret_cast<uint4 *>(p.y) + tok[g] * nv + rank * vpt +
+                                      o % vpt,
                                   pack8(acc));
+                    }
                 }
-                __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mbar_arrive(bar(bEmpty(slot[j])));
-                }
+            }
+            // pre of this parity fully read by this warp
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bColDone(b)));
+            if (collapse_index(warp) == 0) {
+                bool okc = wait_bar<false>(bar(bColDone(b)), use & 1, abort, p.err);
+                if (!__all_sync(0xFFFFFFFFu, okc)) break;
+                if (lane < kCluster) mbar_arrive_remote(mapa(bar(bPreFree(b)), (uint32_t)lane));
             }
         }
     }
@@ -787,7 +762,7 @@ const DevState &dev_state(const DeviceInfo &di) {
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
     if (encode_fn() == nullptr) return st;
-    const size_t smem = smem_bytes(4 * 5);
+    const size_t smem = smem_bytes(kMaxNcc);
     if (cudaFuncSetAttribute(k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
         return st;
@@ -823,7 +798,7 @@ bool path_forced_general() {
 }  // namespace
 
 bool fused_supported(int hc, int64_t d, const DeviceInfo &di) {
-    if (hc != 4 || d % (kCluster * 64) != 0 || d < 2 * kCluster * 64 || d > 5 * kCluster * 64)
+    if (hc != 4 || d % (kCluster * 64) != 0 || d < kCluster * 64 || d > kMaxNcc * kCluster * 64)
         return false;
     if (path_forced_general()) return false;
     return dev_state(di).ok;
@@ -836,12 +811,15 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     const DevState &st = dev_state(di);
     if (!st.ok || hc != 4 || n >= (int64_t(1) << 31)) return cudaErrorNotSupported;
     const int64_t F = 4 * d;
+    const int ncc = (int)(d / (kCluster * 64));
+    // 3-D view of x: {64 channels, token, 64-channel chunk}; one box = one
+    // copy's ncc chunks of 64 tokens, landing as ncc swizzled sub-tiles.
     CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {(cuuint64_t)F, (cuuint64_t)n};
-    const cuuint64_t gstride[1] = {(cuuint64_t)(F * 2)};
-    const cuuint32_t box[2] = {64, kTM};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult r = encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const cuuint64_t gdim[3] = {64, (cuuint64_t)n, (cuuint64_t)(F / 64)};
+    const cuuint64_t gstride[2] = {(cuuint64_t)(F * 2), 128};
+    const cuuint32_t box[3] = {64, kTM, (cuuint32_t)ncc};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                              const_cast<uint16_t *>(x), gdim, gstride, box, estride,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -850,14 +828,14 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     FusedParams p;
     p.n = n;
     p.d = (int)d;
-    p.ncc = (int)(d / (kCluster * 64));
-    p.nkc = 4 * p.ncc;
+    p.ncc = ncc;
     p.num_tiles = (int)((n + kTM - 1) / kTM);
     p.iters = iters;
     p.mixes_only = pre == nullptr ? 1 : 0;
     p.eps = eps;
     p.norm_eps = norm_eps;
     p.F = (float)F;
+    p.x = x;
     p.w = w;
     p.scale = scale;
     p.base = base;
@@ -871,7 +849,7 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes(p.nkc);
+    cfg.dynamicSmemBytes = smem_bytes(p.ncc);
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;

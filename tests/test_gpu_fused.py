@@ -1,5 +1,5 @@
 """The fused tensor-core path of hc_mixes_pre / hc_mixes (hc=4, d a multiple
-of 1024 in [2048, 5120]): it is the path taken (one launch per call), it
+of 1024 in [1024, 5120]): it is the path taken (one launch per call), it
 matches the oracle stage by stage on ragged and multi-tile token counts, and
 it agrees with the general three-kernel path on the same inputs."""
 import os
@@ -61,7 +61,7 @@ def check_all(x, w, sc, base, y, pre, post, comb, m, iters=20, idx=None):
 
 
 @pytest.mark.parametrize("n,d", [(64, 5120), (1, 5120), (70, 5120), (200, 2048),
-                                 (129, 3072), (1000, 4096)])
+                                 (129, 3072), (1000, 4096), (100, 1024), (3000, 5120)])
 def test_fused_small_and_ragged(hc, n, d):
     x, w, sc, base = case(n, d, seed=n + d)
     before = hc.hc_launch_count()
