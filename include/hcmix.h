@@ -152,6 +152,43 @@ size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
  */
 hc_status hc_device_error(unsigned int *flags, int clear);
 
+/* Device floats that libhcmix.so keeps for hc_mixes_pre_noalloc: a fixed
+ * array of 4 MiB on every GPU that loads the library, held until exit. */
+#define HC_NOALLOC_SCRATCH_FLOATS (1u << 20)
+
+/*
+ * hc_mixes_pre_noalloc -- hc_mixes_pre for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point; it exists for
+ * this library's users only.
+ *
+ * Some callers may not call cudaMalloc at all: an engine or plugin host that
+ * owns every device allocation and hands its plugins only input and output
+ * buffers, a framework capturing a region into a CUDA graph where allocation
+ * is forbidden, an allocator's own callbacks, or a real-time loop that must
+ * never reach the allocator.  hc_mixes_pre needs a workspace for the mix
+ * numbers when the caller does not want them; this call keeps them instead in
+ * a fixed array compiled into the library (HC_NOALLOC_SCRATCH_FLOATS floats),
+ * and otherwise computes what hc_mixes_pre computes with mixes == NULL, always
+ * with the general three-kernel path (projection, split/Sinkhorn, collapse).
+ *
+ * Arguments, layouts and validation are those of hc_mixes_pre without mixes
+ * and workspace.  n * (2+hc)*hc must not exceed HC_NOALLOC_SCRATCH_FLOATS
+ * (43,690 tokens at hc = 4, 13,107 at hc = 8); larger n is rejected with
+ * HC_ERR_UNSUPPORTED before anything is enqueued.  The call allocates and
+ * frees nothing.
+ *
+ * The first call on a device looks up the device address of the array on the
+ * current device (cudaGetSymbolAddress), so make that first call before any
+ * stream capture.  All calls share the one array per device: calls that
+ * overlap on the GPU (different streams, or unordered work from different
+ * threads) race on it and must be ordered by the caller.  Each call writes
+ * every scratch element it reads, so nothing needs clearing between calls.
+ */
+hc_status hc_mixes_pre_noalloc(int64_t n, int hc, int64_t d, int iters, float eps,
+                               float norm_eps, const uint16_t *x, const float *w_mix,
+                               const float *hc_scale, const float *hc_base, float *pre,
+                               float *post, float *comb, uint16_t *y, hc_stream_t stream);
+
 /* Number of kernels this library has enqueued in this process (all devices,
  * all threads) since it was loaded.  Host-only counter for diagnostics. */
 uint64_t hc_launch_count(void);
