@@ -56,6 +56,10 @@ constexpr int kRec = 28;                 // floats per partial record (24 + ssq 
 constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
+// The producer runs at most kLag tiles ahead of this CTA's collapse, which
+// re-reads every tile from L2 and so needs it to still be there.
+constexpr int kLag = 3;
+constexpr int kColDoneBufs = 4;  // > kLag: the awaited phase is unambiguous
 
 // warp roles (16 warps: 512 threads leave 128 registers per thread)
 constexpr int kWarpProducer = 0;
@@ -279,9 +283,9 @@ __host__ __device__ constexpr int bRecvFull(int b) { return 2 * kSlots + 8 + b; 
 __host__ __device__ constexpr int bRecvFree(int b) { return 2 * kSlots + 10 + b; }
 __host__ __device__ constexpr int bPreFull(int b) { return 2 * kSlots + 12 + b; }
 __host__ __device__ constexpr int bPreFree(int b) { return 2 * kSlots + 14 + b; }
-__host__ __device__ constexpr int bColDone(int b) { return 2 * kSlots + 16 + b; }
-constexpr int kMmaDrain = 2 * kSlots + 18;
-constexpr int kNumBars = 2 * kSlots + 19;
+__host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 16 + i; }
+constexpr int kMmaDrain = 2 * kSlots + 16 + kColDoneBufs;
+constexpr int kNumBars = kMmaDrain + 1;
 // Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
 constexpr int kEmptyArrivals = 5;
 
@@ -327,10 +331,13 @@ __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams
 
 // ---------------------------------------------------------------- kernel
 
+// NCC = w / 64 (64-channel sub-tiles per copy per CTA) is a template
+// parameter so that all index arithmetic is by constants.
+template <int NCC>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap tmap, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
-    const int ncc = p.ncc;
+    constexpr int ncc = NCC;
     const Smem sm = carve(smem_raw, ncc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
@@ -359,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bRecvFree(b)), kCluster);
             mbar_init(bar(bPreFull(b)), kCluster);
             mbar_init(bar(bPreFree(b)), kCluster);
-            mbar_init(bar(bColDone(b)), kCollapseWarps);
         }
+        for (int i = 0; i < kColDoneBufs; ++i) mbar_init(bar(bColDone(i)), kCollapseWarps);
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -419,6 +426,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int it = 0; it < T && ok; ++it) {
                 const int tile = cluster + it * nclusters;
+                // Stay at most kLag tiles ahead of this CTA's collapse: it
+                // re-reads each tile from L2, which holds it only for a bounded
+                // window.  Tile it-kLag uses col_done buffer (it-kLag) % 4; the
+                // next tile on that buffer is not loaded yet, so the awaited
+                // phase is the only one that can be pending.
+                if (!mixes_only && it >= kLag) {
+                    const int tw = it - kLag;
+                    if (!wait_bar<false>(bar(bColDone(tw % kColDoneBufs)),
+                                         (uint32_t)(tw / kColDoneBufs) & 1, abort, p.err))
+                        break;
+                }
                 for (int j = 0; j < 4; ++j) {
                     const uint32_t q = (uint32_t)(4 * it + j);
                     const int slot = (int)(q % kSlots);
@@ -656,8 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 channels at 8*(o % (w/8))) of this CTA's slice; 4 vectors in flight
         // per thread, each needing the 4 copies (16-byte loads from L2).
         const int ct = collapse_index(warp) * 32 + lane;
-        const int vpt = w / 8;  // vectors per token
-        const int nout = kTM * vpt;
+        constexpr int vpt = NCC * 8;  // vectors per token
+        constexpr int nout = kTM * vpt;
         const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
         const int64_t nv = p.d / 8;  // vectors per copy row
         for (int it = 0; it < T; ++it) {
@@ -675,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int o = o0 + g * kCollapseThreads;
                     tok[g] = (int64_t)tile * kTM + o / vpt;
                     if (o < nout && tok[g] < p.n) {
-                        const int64_t v = (int64_t)rank * vpt + o % vpt;
+                        const int v = rank * vpt + o % vpt;
 #pragma unroll
                         for (int j = 0; j < 4; ++j) xv[g][j] = __ldcs(x + (tok[g] * 4 + j) * nv + v);
                     }
@@ -707,9 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // pre of this parity fully read by this warp
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bColDone(b)));
+            if (lane == 0) mbar_arrive(bar(bColDone(it % kColDoneBufs)));
             if (collapse_index(warp) == 0) {
-                bool okc = wait_bar<false>(bar(bColDone(b)), use & 1, abort, p.err);
+                bool okc = wait_bar<false>(bar(bColDone(it % kColDoneBufs)),
+                                           (uint32_t)(it / kColDoneBufs) & 1, abort, p.err);
                 if (!__all_sync(0xFFFFFFFFu, okc)) break;
                 if (lane < kCluster) mbar_arrive_remote(mapa(bar(bPreFree(b)), (uint32_t)lane));
             }
@@ -753,6 +772,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+using FusedKernel = void (*)(CUtensorMap, FusedParams);
+
+// The instantiation for w = 64 * ncc channels per CTA.
+FusedKernel kernel_for(int ncc) {
+    switch (ncc) {
+        case 1: return k_fused<1>;
+        case 2: return k_fused<2>;
+        case 3: return k_fused<3>;
+        case 4: return k_fused<4>;
+        default: return k_fused<5>;
+    }
+}
+
 const DevState &dev_state(const DeviceInfo &di) {
     std::lock_guard<std::mutex> lk(g_fmu);
     DevState &st = g_dev[di.device];
@@ -762,13 +794,15 @@ const DevState &dev_state(const DeviceInfo &di) {
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
     if (encode_fn() == nullptr) return st;
+    for (int ncc = 1; ncc <= kMaxNcc; ++ncc) {
+        if (cudaFuncSetAttribute(kernel_for(ncc), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem_bytes(ncc)) != cudaSuccess)
+            return st;
+        if (cudaFuncSetAttribute(kernel_for(ncc), cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                 1) != cudaSuccess)
+            return st;
+    }
     const size_t smem = smem_bytes(kMaxNcc);
-    if (cudaFuncSetAttribute(k_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-        return st;
-    if (cudaFuncSetAttribute(k_fused, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-        cudaSuccess)
-        return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCluster);
     cfg.blockDim = dim3(kThreads);
@@ -781,7 +815,7 @@ const DevState &dev_state(const DeviceInfo &di) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    if (cudaOccupancyMaxActiveClusters(&nc, k_fused, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&nc, kernel_for(kMaxNcc), &cfg) != cudaSuccess) {
         cudaGetLastError();
         return st;
     }
@@ -858,7 +892,7 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_fused, tmap, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc), tmap, p);
     if (e != cudaSuccess) return e;
     return launched();
 }
