@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(DESCR), default="large")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (small cases for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -231,9 +233,9 @@ def run_ours(args, wl, ws, rank, local):
     build.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    n, H, d = wl.n, wl.hc, wl.d
+    n, H, d = (args.tokens or wl.n), wl.hc, wl.d
     iters = 20 if 20 in wl.iters else wl.iters[0]
-    s = inputs.make_streams(wl, device=dev)
+    s = inputs.make_streams(wl, n=n, device=dev)
     p = inputs.make_params(wl, device=dev)
     x, out = s["x"], s["out"]
     pre = torch.empty((n, H), device=dev)
@@ -352,7 +354,9 @@ def run_ours(args, wl, ws, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": DESCR[args.workload], "tokens": n, "hc": H, "d": d,
+        "config": {"workload": DESCR[args.workload] + (
+                       "" if n == wl.n else " [token count overridden: %d]" % n),
+                   "tokens": n, "hc": H, "d": d,
                    "iters": iters, "l2": ("flushed between steps (%d MB write)" %
                                           (2 * L2_BYTES >> 20)) if flush is not None
                    else "inputs larger than L2 (stream %.2f GB), no flush" % (x.numel() * 2 / 1e9),
