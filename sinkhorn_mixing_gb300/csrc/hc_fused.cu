@@ -19,12 +19,12 @@
 //   * At the end of a tile each CTA sends its 24 partial mix numbers and
 //     partial sum of squares per token to the token's owner CTA (4 tokens per
 //     CTA) through distributed shared memory.  The owner warp reduces the 16
-//     records in a fixed order, forms r and m, runs the split + Sinkhorn,
-//     writes pre/post/comb (and m) and broadcasts pre to all 16 CTAs.
-//   * The collapse y = sum_j pre_j x_j re-reads the tile's x slice with
-//     16-byte loads (the bytes were fetched from HBM by the TMA a few
-//     microseconds earlier and are served by L2) and writes y; when done it
-//     releases its pre buffer to every owner.
+//     records in a fixed order, forms r and m, computes pre (and then post and
+//     the Sinkhorn comb) and writes them out.
+//   * The owner CTA also collapses its own tokens: y = sum_j pre_j x_j over
+//     all d channels of its 4 tokens, re-reading their rows with 16-byte loads
+//     (the bytes were fetched from HBM by the cluster's TMA a few microseconds
+//     earlier and are served by L2).  pre never leaves the CTA.
 //   Every consumer of the ring (MMA thread, 4 square warps) waits on and
 //   releases every stage in order, so each wait is for the phase right after
 //   one it has already seen.
@@ -60,6 +60,7 @@ constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 // re-reads every tile from L2 and so needs it to still be there.
 constexpr int kLag = 3;
 constexpr int kColDoneBufs = 4;  // > kLag: the awaited phase is unambiguous
+static_assert(kColDoneBufs > kLag, "pre staging and col_done must outlive the lag");
 
 // warp roles (16 warps: 512 threads leave 128 registers per thread)
 constexpr int kWarpProducer = 0;
@@ -264,9 +265,8 @@ struct Smem {
     uint8_t *w;       // 4*ncc chunks of [48 x 64] bf16, swizzled, chunk = copy*ncc + cc
     uint8_t *ring;    // kSlots stages of ncc sub-tiles [64 x 64] bf16, swizzled
     float *recv;      // [2][kCluster][kOwn][kRec]   partials received as owner
-    float *pre;       // [2][kTM][4]                 pre of the tile's tokens
     float *sq;        // [2][kTM]                    this CTA's partial sums of squares
-    float *stage;     // [kOwn][4]                   pre of the owned tokens
+    float *stage;     // [kColDoneBufs][kOwn][4]     pre of the owned tokens, by tile % 4
     uint64_t *bar;    // barriers, see below
     uint32_t *tmem;   // TMEM base address written by tcgen05.alloc
     int *abort;
@@ -281,10 +281,9 @@ __host__ __device__ constexpr int bSqFull(int b) { return 2 * kSlots + 4 + b; }
 __host__ __device__ constexpr int bSqEmpty(int b) { return 2 * kSlots + 6 + b; }
 __host__ __device__ constexpr int bRecvFull(int b) { return 2 * kSlots + 8 + b; }
 __host__ __device__ constexpr int bRecvFree(int b) { return 2 * kSlots + 10 + b; }
-__host__ __device__ constexpr int bPreFull(int b) { return 2 * kSlots + 12 + b; }
-__host__ __device__ constexpr int bPreFree(int b) { return 2 * kSlots + 14 + b; }
-__host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 16 + i; }
-constexpr int kMmaDrain = 2 * kSlots + 16 + kColDoneBufs;
+__host__ __device__ constexpr int bPreReady(int i) { return 2 * kSlots + 12 + i; }
+__host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 12 + kColDoneBufs + i; }
+constexpr int kMmaDrain = 2 * kSlots + 12 + 2 * kColDoneBufs;
 constexpr int kNumBars = kMmaDrain + 1;
 // Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
 constexpr int kEmptyArrivals = 5;
@@ -293,7 +292,7 @@ __host__ __device__ constexpr size_t ring_bytes(int ncc) { return (size_t)kSlots
 
 __host__ __device__ constexpr size_t smem_bytes(int ncc) {
     return 1024 /* alignment slack */ + (size_t)4 * ncc * kWChunkBytes + ring_bytes(ncc) +
-           2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 * 4 + 2 * kTM * 4 + kOwn * 4 * 4 +
+           2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 + kColDoneBufs * kOwn * 4 * 4 +
            kNumBars * 8 + 16;
 }
 
@@ -309,12 +308,10 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
     // 64..127, never used): the records that follow are at least that large.
     s.recv = reinterpret_cast<float *>(p);
     p += 2 * kCluster * kOwn * kRec * 4;
-    s.pre = reinterpret_cast<float *>(p);
-    p += 2 * kTM * 4 * 4;
     s.sq = reinterpret_cast<float *>(p);
     p += 2 * kTM * 4;
     s.stage = reinterpret_cast<float *>(p);
-    p += kOwn * 4 * 4;
+    p += kColDoneBufs * kOwn * 4 * 4;
     s.bar = reinterpret_cast<uint64_t *>(p);
     p += kNumBars * 8;
     s.tmem = reinterpret_cast<uint32_t *>(p);
@@ -364,10 +361,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bSqEmpty(b)), 2);
             mbar_init(bar(bRecvFull(b)), kCluster * kOwn);
             mbar_init(bar(bRecvFree(b)), kCluster);
-            mbar_init(bar(bPreFull(b)), kCluster);
-            mbar_init(bar(bPreFree(b)), kCluster);
         }
-        for (int i = 0; i < kColDoneBufs; ++i) mbar_init(bar(bColDone(i)), kCollapseWarps);
+        for (int i = 0; i < kColDoneBufs; ++i) {
+            mbar_init(bar(bPreReady(i)), 1);
+            mbar_init(bar(bColDone(i)), kCollapseWarps);
+        }
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -610,9 +608,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ssum += r4[6].x;
                 }
             }
-            __syncwarp();
-            // all records of this parity read: release them to every sender
-            if (lane < kCluster) mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)lane));
             float pr[4], po[4];
             int64_t t = 0;
             if (lane < kOwn) {
@@ -627,29 +622,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         dst[v] = make_float4(m[4 * v], m[4 * v + 1], m[4 * v + 2], m[4 * v + 3]);
                 }
                 if (!mixes_only) {
+                    // stage[it % 4] was last read by the collapse of tile it-4,
+                    // which finished before the producer loaded tile it-1
+                    // (the producer stays at most kLag = 3 tiles ahead).
                     split_pre_post<4>([&](int k) { return m[k]; }, [&](int k) { return bse[k]; },
                                       s0, s1, p.eps, pr, po);
-                    reinterpret_cast<float4 *>(sm.stage)[lane] =
+                    reinterpret_cast<float4 *>(sm.stage)[(it % kColDoneBufs) * kOwn + lane] =
                         make_float4(pr[0], pr[1], pr[2], pr[3]);
                 }
             }
             __syncwarp();
+            // pre first: this CTA's collapse waits for it
+            if (!mixes_only && lane == 0) mbar_arrive(bar(bPreReady(it % kColDoneBufs)));
+            // All records of this parity are read: release them to every
+            // sender.  Lanes 16..31 issue these release-ordered arrives: they
+            // have no global stores pending for the release to wait on.
+            if (lane >= 32 - kCluster)
+                mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)(lane - (32 - kCluster))));
             if (!mixes_only) {
-                // pre first (the collapse waits for it); every CTA must have
-                // finished reading this parity's pre buffer
-                bool okf = true;
-                if (lane < kCluster)
-                    okf = wait_bar<true>(bar(bPreFree(b)), (use & 1) ^ 1, abort, p.err);
-                if (!__all_sync(0xFFFFFFFFu, okf)) break;
-                if (lane < kCluster) {
-                    const uint32_t pa = su32(sm.pre + (b * kTM + rank * kOwn) * 4);
-#pragma unroll
-                    for (int uu = 0; uu < kOwn; ++uu) {
-                        const float4 v4 = reinterpret_cast<const float4 *>(sm.stage)[uu];
-                        st_cluster_v4(mapa(pa + 16 * uu, (uint32_t)lane), v4.x, v4.y, v4.z, v4.w);
-                    }
-                    mbar_arrive_remote(mapa(bar(bPreFull(b)), (uint32_t)lane));
-                }
                 // then the Sinkhorn for comb, off the collapse's critical path
                 if (lane < kOwn) {
                     float Cm[4][4];
@@ -670,40 +660,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
     } else if (!mixes_only) {
-        // Collapse: 7 warps, 224 threads.  Output vector o = (token o / (w/8),
-        // 8 channels at 8*(o % (w/8))) of this CTA's slice; 4 vectors in flight
+        // Collapse of this CTA's own tokens rank*kOwn + u (u < kOwn) of every
+        // tile, over all d channels: 7 warps, 224 threads.  Output vector
+        // o = (token u = o / nv, 8 channels at 8*(o % nv)); 4 vectors in flight
         // per thread, each needing the 4 copies (16-byte loads from L2).
         const int ct = collapse_index(warp) * 32 + lane;
-        constexpr int vpt = NCC * 8;  // vectors per token
-        constexpr int nout = kTM * vpt;
+        constexpr int nv = NCC * 8 * kCluster;  // vectors per copy row (d / 8)
+        constexpr int nout = kOwn * nv;
         const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
-        const int64_t nv = p.d / 8;  // vectors per copy row
         for (int it = 0; it < T; ++it) {
-            const int b = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
             const int tile = cluster + it * nclusters;
-            if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(bPreFull(b)), use & 1, abort, p.err)))
+            const int ib = it % kColDoneBufs;
+            if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bPreReady(ib)),
+                                                         (uint32_t)(it / kColDoneBufs) & 1, abort,
+                                                         p.err)))
                 break;
+            const int64_t tok0 = (int64_t)tile * kTM + rank * kOwn;
             constexpr int G = 4;
             for (int o0 = ct; o0 < nout; o0 += G * kCollapseThreads) {
                 uint4 xv[G][4];
-                int64_t tok[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const int o = o0 + g * kCollapseThreads;
-                    tok[g] = (int64_t)tile * kTM + o / vpt;
-                    if (o < nout && tok[g] < p.n) {
-                        const int v = rank * vpt + o % vpt;
+                    const int64_t tok = tok0 + o / nv;
+                    if (o < nout && tok < p.n) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) xv[g][j] = __ldcs(x + (tok[g] * 4 + j) * nv + v);
+                        for (int j = 0; j < 4; ++j)
+                            xv[g][j] = __ldcs(x + (tok * 4 + j) * nv + o % nv);
                     }
                 }
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const int o = o0 + g * kCollapseThreads;
-                    if (o < nout && tok[g] < p.n) {
-                        const float4 pr =
-                            *reinterpret_cast<const float4 *>(sm.pre + (b * kTM + o / vpt) * 4);
+                    const int64_t tok = tok0 + o / nv;
+                    if (o < nout && tok < p.n) {
+                        const float4 pr = reinterpret_cast<const float4 *>(
+                            sm.stage)[ib * kOwn + o / nv];
                         float acc[8], f[8];
                         unpack8(xv[g][0], f);
 #pragma unroll
@@ -717,21 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         unpack8(xv[g][3], f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
-                        st_stream(reinterpret_cast<uint4 *>(p.y) + tok[g] * nv + rank * vpt +
-                                      o % vpt,
-                                  pack8(acc));
+                        st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + o % nv, pack8(acc));
                     }
                 }
             }
-            // pre of this parity fully read by this warp
+            // this warp is done with tile it (its pre slot and its L2 lines)
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bColDone(it % kColDoneBufs)));
-            if (collapse_index(warp) == 0) {
-                bool okc = wait_bar<false>(bar(bColDone(it % kColDoneBufs)),
-                                           (uint32_t)(it / kColDoneBufs) & 1, abort, p.err);
-                if (!__all_sync(0xFFFFFFFFu, okc)) break;
-                if (lane < kCluster) mbar_arrive_remote(mapa(bar(bPreFree(b)), (uint32_t)lane));
-            }
+            if (lane == 0) mbar_arrive(bar(bColDone(ib)));
         }
     }
 
