@@ -9,16 +9,20 @@
 //   * The CTA keeps its slice of W_mix resident in shared memory for the whole
 //     kernel, split into bf16 hi + lo rows (48 rows = 24 hi, 24 lo), in the
 //     128-byte-swizzled K-major layout the tensor core reads.
-//   * x streams through a 2-slot ring: one TMA operation per (tile, copy)
-//     brings the copy's w channels of the tile's 64 tokens (w/64 swizzled
-//     [64 x 64] sub-tiles, 40 KB at d = 5120).  Few, large TMA operations
-//     matter: the per-CTA rate of TMA operations, not their size, bounds the
-//     bandwidth of small boxes.  Per sub-tile, 4 tcgen05.mma (M=128 rows of
-//     which the 64 tokens are the first half, N=48, K=16) accumulate
-//     x.(W_hi + W_lo) in TMEM (binary32); 4 square warps add x^2 per token.
+//   * x streams through a 3-slot ring: one TMA operation per (tile, 64-channel
+//     chunk) brings that chunk of all 4 copies of the tile's 64 tokens (4
+//     swizzled [64 x 64] sub-tiles, 32 KB).  Few, large TMA operations matter:
+//     the per-CTA rate of TMA operations, not their size, bounds the bandwidth
+//     of small boxes; three slots keep two loads in flight while the third is
+//     consumed.  Per sub-tile, 4 tcgen05.mma (M=128 rows of which the 64 tokens
+//     are the first half, N=48, K=16) accumulate x.(W_hi + W_lo) in TMEM
+//     (binary32); 4 square warps add x^2 per token.
 //   * At the end of a tile each CTA sends its 24 partial mix numbers and
 //     partial sum of squares per token to the token's owner CTA (4 tokens per
-//     CTA) through distributed shared memory.  The owner warp reduces the 16
+//     CTA) with asynchronous distributed-shared-memory stores whose bytes
+//     complete the owner's barrier; the owner hands the buffer back with a
+//     relaxed remote arrive (a release-ordered one waits for the SM's memory
+//     traffic and cost microseconds per tile).  The owner warp reduces the 16
 //     records in a fixed order, forms r and m, computes pre (and then post and
 //     the Sinkhorn comb) and writes them out.
 //   * The owner CTA also collapses its own tokens: y = sum_j pre_j x_j over
@@ -48,11 +52,14 @@ constexpr int kCluster = 16;             // CTAs per cluster
 constexpr int kTM = 64;                  // tokens per tile
 constexpr int kMix = 24;                 // (2 + 4) * 4
 constexpr int kNW = 48;                  // B rows: 24 hi + 24 lo
-constexpr int kSlots = 2;                // x ring depth (one copy of a tile per slot)
+constexpr int kSlots = 3;                // x ring depth (one 64-channel chunk of a tile per slot)
 constexpr int kSubBytes = kTM * 128;     // one swizzled [64 tokens x 64 channels] sub-tile
+constexpr int kStageBytes = 4 * kSubBytes;  // the 4 copies' sub-tiles of one chunk
 constexpr int kWChunkBytes = kNW * 128;  // one [48 x 64] bf16 chunk of W
 constexpr int kOwn = kTM / kCluster;     // tokens owned per CTA per tile
 constexpr int kRec = 28;                 // floats per partial record (24 + ssq + pad)
+// bytes of records one owner receives per tile: 16 senders x 4 tokens x 7 x 16 B
+constexpr uint32_t kRecvTx = kCluster * kOwn * 7 * 16;
 constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
 constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
@@ -128,9 +135,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar, uint32_t count = 1) {
                  : "memory");
 }
 
-// Arrive on a barrier of another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+// Arrive on a barrier of another CTA of the cluster (address from mapa),
+// without release ordering: a cluster-scope release waits for the memory
+// traffic still in flight, which costs microseconds on a streaming SM.  Used
+// only where every access the arrive must follow has already completed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                      cluster_addr)
                  : "memory");
 }
@@ -183,10 +193,15 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
+// Asynchronous 16-byte store into another CTA's shared memory; its bytes
+// complete a transaction count on the destination CTA's barrier `bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -195,12 +210,12 @@ __device__ __forceinline__ void cluster_sync_all() {
                      : "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, uint32_t bar) {
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
 
@@ -262,9 +277,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // ---------------------------------------------------------------- layout
 
 struct Smem {
+    uint8_t *ring;    // kSlots stages of 4 sub-tiles [64 x 64] bf16 (one per copy), swizzled
     uint8_t *w;       // 4*ncc chunks of [48 x 64] bf16, swizzled, chunk = copy*ncc + cc
-    uint8_t *ring;    // kSlots stages of ncc sub-tiles [64 x 64] bf16, swizzled
-    float *recv;      // [2][kCluster][kOwn][kRec]   partials received as owner
+    float *recv;      // [kCluster][kOwn][kRec]      partials received as owner
     float *sq;        // [2][kTM]                    this CTA's partial sums of squares
     float *stage;     // [kColDoneBufs][kOwn][4]     pre of the owned tokens, by tile % 4
     uint64_t *bar;    // barriers, see below
@@ -279,35 +294,35 @@ __host__ __device__ constexpr int bAccFull(int b) { return 2 * kSlots + b; }
 __host__ __device__ constexpr int bAccEmpty(int b) { return 2 * kSlots + 2 + b; }
 __host__ __device__ constexpr int bSqFull(int b) { return 2 * kSlots + 4 + b; }
 __host__ __device__ constexpr int bSqEmpty(int b) { return 2 * kSlots + 6 + b; }
-__host__ __device__ constexpr int bRecvFull(int b) { return 2 * kSlots + 8 + b; }
-__host__ __device__ constexpr int bRecvFree(int b) { return 2 * kSlots + 10 + b; }
-__host__ __device__ constexpr int bPreReady(int i) { return 2 * kSlots + 12 + i; }
-__host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 12 + kColDoneBufs + i; }
-constexpr int kMmaDrain = 2 * kSlots + 12 + 2 * kColDoneBufs;
+constexpr int kRecvFull = 2 * kSlots + 8;
+constexpr int kRecvFree = 2 * kSlots + 9;
+__host__ __device__ constexpr int bPreReady(int i) { return 2 * kSlots + 10 + i; }
+__host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 10 + kColDoneBufs + i; }
+constexpr int kMmaDrain = 2 * kSlots + 10 + 2 * kColDoneBufs;
 constexpr int kNumBars = kMmaDrain + 1;
 // Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
 constexpr int kEmptyArrivals = 5;
 
-__host__ __device__ constexpr size_t ring_bytes(int ncc) { return (size_t)kSlots * ncc * kSubBytes; }
+constexpr size_t kRingBytes = (size_t)kSlots * kStageBytes;
+constexpr size_t kRecvBytes = (size_t)kCluster * kOwn * kRec * 4;
 
 __host__ __device__ constexpr size_t smem_bytes(int ncc) {
-    return 1024 /* alignment slack */ + (size_t)4 * ncc * kWChunkBytes + ring_bytes(ncc) +
-           2 * kCluster * kOwn * kRec * 4 + 2 * kTM * 4 + kColDoneBufs * kOwn * 4 * 4 +
-           kNumBars * 8 + 16;
+    return 1024 /* alignment slack */ + kRingBytes + (size_t)4 * ncc * kWChunkBytes + kRecvBytes +
+           2 * kTM * 4 + kColDoneBufs * kOwn * 4 * 4 + kNumBars * 8 + 16;
 }
 
 __device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
     uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023;
     uint8_t *p = reinterpret_cast<uint8_t *>(a);
     Smem s;
+    s.ring = p;
+    p += kRingBytes;
+    // The M=128 operand of the last sub-tile reads 8 KB past the ring (rows
+    // 64..127, never used): W, which follows, is at least that large.
     s.w = p;
     p += (size_t)4 * ncc * kWChunkBytes;
-    s.ring = p;
-    p += ring_bytes(ncc);
-    // The M=128 operand of the last sub-tile reads 8 KB past the ring (rows
-    // 64..127, never used): the records that follow are at least that large.
     s.recv = reinterpret_cast<float *>(p);
-    p += 2 * kCluster * kOwn * kRec * 4;
+    p += kRecvBytes;
     s.sq = reinterpret_cast<float *>(p);
     p += 2 * kTM * 4;
     s.stage = reinterpret_cast<float *>(p);
@@ -318,7 +333,8 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
     s.abort = reinterpret_cast<int *>(p + 4);
     return s;
 }
-static_assert(2 * kCluster * kOwn * kRec * 4 >= kSubBytes, "overrun of the last sub-tile");
+static_assert(4 * kWChunkBytes >= kSubBytes, "overrun of the last sub-tile");
+static_assert(kStageBytes % 1024 == 0 && kWChunkBytes % 1024 == 0, "swizzle atoms stay aligned");
 
 // First feature (within the token's F) of W chunk kc = copy*ncc + cc of CTA `rank`.
 __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams &p) {
@@ -340,8 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rank = (int)(blockIdx.x % kCluster);
     const int cluster = (int)(blockIdx.x / kCluster);
     const int nclusters = (int)(gridDim.x / kCluster);
-    const int w = ncc * 64;
-    const uint32_t stage_bytes = (uint32_t)ncc * kSubBytes;
     const bool mixes_only = p.mixes_only != 0;
     const int T = cluster < p.num_tiles ? (p.num_tiles - cluster + nclusters - 1) / nclusters : 0;
     volatile int *abort = sm.abort;
@@ -359,15 +373,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bAccEmpty(b)), 2);
             mbar_init(bar(bSqFull(b)), 4);
             mbar_init(bar(bSqEmpty(b)), 2);
-            mbar_init(bar(bRecvFull(b)), kCluster * kOwn);
-            mbar_init(bar(bRecvFree(b)), kCluster);
         }
+        mbar_init(bar(kRecvFull), 1);
+        mbar_init(bar(kRecvFree), kCluster);
         for (int i = 0; i < kColDoneBufs; ++i) {
             mbar_init(bar(bPreReady(i)), 1);
             mbar_init(bar(bColDone(i)), kCollapseWarps);
         }
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_expect_tx(bar(kRecvFull), kRecvTx);
     }
     if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -418,9 +433,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ------------------------------------------------------------ roles
     if (warp == kWarpProducer) {
-        // stage q = 4*it + copy: the copy's w channels of the tile's 64 tokens
+        // stage q = ncc*it + cc: chunk cc of this CTA's channels, all 4 copies
         if (lane == 0) {
-            int last_use[kSlots] = {-1, -1};
+            int last_use[kSlots] = {-1, -1, -1};
             bool ok = true;
             for (int it = 0; it < T && ok; ++it) {
                 const int tile = cluster + it * nclusters;
@@ -435,17 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          (uint32_t)(tw / kColDoneBufs) & 1, abort, p.err))
                         break;
                 }
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t q = (uint32_t)(4 * it + j);
+                for (int cc = 0; cc < ncc; ++cc) {
+                    const uint32_t q = (uint32_t)(ncc * it + cc);
                     const int slot = (int)(q % kSlots);
                     const uint32_t use = q / kSlots;
                     if (!wait_bar<false>(bar(bEmpty(slot)), (use & 1) ^ 1, abort, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(bFull(slot)), stage_bytes);
-                    tma_load_3d(su32(sm.ring + slot * stage_bytes), &tmap, 0, tile * kTM,
-                                (j * p.d + rank * w) / 64, bar(bFull(slot)));
+                    mbar_expect_tx(bar(bFull(slot)), kStageBytes);
+                    tma_load_4d(su32(sm.ring + slot * kStageBytes), &tmap, 0, tile * kTM,
+                                rank * ncc + cc, 0, bar(bFull(slot)));
                     last_use[slot] = (int)use;
                 }
             }
@@ -463,22 +478,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t q = (uint32_t)(4 * it + j);
+                for (int cc = 0; cc < ncc; ++cc) {
+                    const uint32_t q = (uint32_t)(ncc * it + cc);
                     const int slot = (int)(q % kSlots);
                     if (!wait_bar<false>(bar(bFull(slot)), (q / kSlots) & 1, abort, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = su32(sm.ring + slot * stage_bytes);
-                    const uint32_t b0 = su32(sm.w + (size_t)(j * ncc) * kWChunkBytes);
-                    for (int cc = 0; cc < ncc; ++cc) {
+                    const uint32_t a0 = su32(sm.ring + slot * kStageBytes);
+                    const uint32_t b0 = su32(sm.w + (size_t)cc * kWChunkBytes);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            mma_bf16(d_tmem, sw128_desc(a0 + cc * kSubBytes + 32 * k),
-                                     sw128_desc(b0 + cc * kWChunkBytes + 32 * k),
-                                     (j | cc | k) != 0);
+                            mma_bf16(d_tmem, sw128_desc(a0 + j * kSubBytes + 32 * k),
+                                     sw128_desc(b0 + j * ncc * kWChunkBytes + 32 * k),
+                                     (cc | j | k) != 0);
                     }
                     mma_commit(bar(bEmpty(slot)));
                 }
@@ -499,21 +515,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
             float ss = 0.f;
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t q = (uint32_t)(4 * it + j);
+            for (int cc = 0; cc < ncc; ++cc) {
+                const uint32_t q = (uint32_t)(ncc * it + cc);
                 const int slot = (int)(q % kSlots);
                 if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(bFull(slot)), (q / kSlots) & 1,
                                                              abort, p.err))) {
                     ok = false;
                     break;
                 }
-                const uint32_t base = su32(sm.ring + slot * stage_bytes) + i * 128;
-                for (int cc = 0; cc < ncc; ++cc) {
+                const uint32_t base = su32(sm.ring + slot * kStageBytes) + i * 128;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         // chunk (4h+m) ^ (row & 7): 8 consecutive lanes hit 8 bank groups
                         float f[8];
-                        unpack8(lds128(base + cc * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4)), f);
+                        unpack8(lds128(base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4)), f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
                     }
@@ -554,26 +571,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float ss = sm.sq[b * kTM + i];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bSqEmpty(b)));
-            // the owner's record slot for this tile parity must be free
+            // the owner must have read the records of the previous tile
             if (!__all_sync(0xFFFFFFFFu,
-                            wait_bar<true>(bar(bRecvFree(b)), (use & 1) ^ 1, abort, p.err)))
+                            wait_bar<true>(bar(kRecvFree), ((uint32_t)it & 1) ^ 1, abort, p.err)))
                 break;
             const uint32_t rec =
-                mapa(su32(sm.recv + ((b * kCluster + rank) * kOwn + u) * kRec), (uint32_t)owner);
+                mapa(su32(sm.recv + (rank * kOwn + u) * kRec), (uint32_t)owner);
+            // 7 asynchronous stores; their bytes complete the owner's recv_full
+            const uint32_t rfull = mapa(bar(kRecvFull), (uint32_t)owner);
 #pragma unroll
             for (int v = 0; v < 6; ++v)
-                st_cluster_v4(rec + 16 * v, acc[4 * v] + acc[24 + 4 * v],
-                              acc[4 * v + 1] + acc[24 + 4 * v + 1],
-                              acc[4 * v + 2] + acc[24 + 4 * v + 2],
-                              acc[4 * v + 3] + acc[24 + 4 * v + 3]);
-            st_cluster_v4(rec + 96, ss, 0.f, 0.f, 0.f);
-            mbar_arrive_remote(mapa(bar(bRecvFull(b)), (uint32_t)owner));
+                st_async_v4(rec + 16 * v, acc[4 * v] + acc[24 + 4 * v],
+                            acc[4 * v + 1] + acc[24 + 4 * v + 1],
+                            acc[4 * v + 2] + acc[24 + 4 * v + 2],
+                            acc[4 * v + 3] + acc[24 + 4 * v + 3], rfull);
+            st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
         }
     } else if (warp == kWarpOwner) {
         // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: lanes u < kOwn
-        // reduce the 16 records of their token in a fixed order, form r and m,
-        // run split + Sinkhorn; lanes 0..15 then release the record slots and
-        // deliver pre to CTA `lane`, one release-ordered arrive each.
+        // reduce the 16 records of their token in a fixed order, form r, m and
+        // pre for this CTA's collapse; lanes 16..31 then hand the record buffer
+        // back to the 16 senders, and lanes u < kOwn run the Sinkhorn for comb.
         float bse[kMix], s0 = 0.f, s1 = 0.f, s2 = 0.f;
         if (!mixes_only && lane < kOwn) {
 #pragma unroll
@@ -583,11 +601,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             s2 = __ldg(p.scale + 2);
         }
         for (int it = 0; it < T; ++it) {
-            const int b = it & 1;
-            const uint32_t use = (uint32_t)(it >> 1);
             const int tile = cluster + it * nclusters;
             if (!__all_sync(0xFFFFFFFFu,
-                            wait_bar<true>(bar(bRecvFull(b)), use & 1, abort, p.err)))
+                            wait_bar<true>(bar(kRecvFull), (uint32_t)it & 1, abort, p.err)))
                 break;
             float m[kMix];
             float ssum = 0.f;
@@ -596,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < kMix; ++k) m[k] = 0.f;
                 for (int src = 0; src < kCluster; ++src) {
                     const float4 *r4 = reinterpret_cast<const float4 *>(
-                        sm.recv + ((b * kCluster + src) * kOwn + lane) * kRec);
+                        sm.recv + (src * kOwn + lane) * kRec);
 #pragma unroll
                     for (int v = 0; v < 6; ++v) {
                         const float4 t4 = r4[v];
@@ -634,11 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             // pre first: this CTA's collapse waits for it
             if (!mixes_only && lane == 0) mbar_arrive(bar(bPreReady(it % kColDoneBufs)));
-            // All records of this parity are read: release them to every
-            // sender.  Lanes 16..31 issue these release-ordered arrives: they
-            // have no global stores pending for the release to wait on.
+            // All records are read (their values are in registers and used
+            // above, so no later store can overtake the loads): arm recv_full
+            // for the next tile's bytes, then release the buffer to every
+            // sender, lanes 16..31 one CTA each.
+            if (lane == 0) mbar_expect_tx(bar(kRecvFull), kRecvTx);
             if (lane >= 32 - kCluster)
-                mbar_arrive_remote(mapa(bar(bRecvFree(b)), (uint32_t)(lane - (32 - kCluster))));
+                mbar_arrive_remote_relaxed(mapa(bar(kRecvFree), (uint32_t)(lane - (32 - kCluster))));
             if (!mixes_only) {
                 // then the Sinkhorn for comb, off the collapse's critical path
                 if (lane < kOwn) {
@@ -830,14 +848,15 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     if (!st.ok || hc != 4 || n >= (int64_t(1) << 31)) return cudaErrorNotSupported;
     const int64_t F = 4 * d;
     const int ncc = (int)(d / (kCluster * 64));
-    // 3-D view of x: {64 channels, token, 64-channel chunk}; one box = one
-    // copy's ncc chunks of 64 tokens, landing as ncc swizzled sub-tiles.
+    // 4-D view of x: {64 channels, token, 64-channel chunk of a copy, copy};
+    // one box = one chunk of all 4 copies of 64 tokens, landing as 4 swizzled
+    // sub-tiles.
     CUtensorMap tmap;
-    const cuuint64_t gdim[3] = {64, (cuuint64_t)n, (cuuint64_t)(F / 64)};
-    const cuuint64_t gstride[2] = {(cuuint64_t)(F * 2), 128};
-    const cuuint32_t box[3] = {64, kTM, (cuuint32_t)ncc};
-    const cuuint32_t estride[3] = {1, 1, 1};
-    CUresult r = encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    const cuuint64_t gdim[4] = {64, (cuuint64_t)n, (cuuint64_t)(d / 64), 4};
+    const cuuint64_t gstride[3] = {(cuuint64_t)(F * 2), 128, (cuuint64_t)(d * 2)};
+    const cuuint32_t box[4] = {64, kTM, 1, 4};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                              const_cast<uint16_t *>(x), gdim, gstride, box, estride,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
