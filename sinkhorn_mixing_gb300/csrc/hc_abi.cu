@@ -1,10 +1,12 @@
 // hc_abi.cu -- the extern "C" entry points of libhcmix.so: host-side argument
 // validation, path selection and launch.  Nothing here allocates memory.
 #include <math.h>
+#include <stdlib.h>
 #include <atomic>
 #include <mutex>
 
 #include "../../include/hcmix.h"
+#include "hc_decode.h"
 #include "hc_fused.h"
 #include "hc_internal.h"
 
@@ -23,6 +25,14 @@ bool g_have[kMaxDevices];
 }  // namespace
 
 void count_launches(int k) { g_launches.fetch_add((uint64_t)k, std::memory_order_relaxed); }
+
+ForcedPath forced_path() {
+    const char *e = getenv("HCMIX_PATH");
+    if (e == nullptr) return kPathAuto;
+    if (e[0] == 'g') return kPathGeneral;
+    if (e[0] == 'f') return kPathFused;
+    return kPathAuto;
+}
 
 cudaError_t device_info(DeviceInfo *out) {
     int dev = 0;
@@ -147,6 +157,11 @@ hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t 
     cudaError_t e = hc::device_info(&di);
     if (e != cudaSuccess) return HC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hc::decode_supported(n, hc, d, di)) {
+        return from_cuda(hc::launch_decode(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
+                                           w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
+                                           nullptr, nullptr, di, s));
+    }
     if (hc::fused_supported(hc, d, di)) {
         return from_cuda(hc::launch_fused(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
                                           w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
@@ -245,6 +260,10 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float
     hc::DeviceInfo di;
     if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hc::decode_supported(n, hc, d, di)) {
+        return from_cuda(hc::launch_decode(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
+                                           hc_base, mixes, pre, post, comb, y, di, s));
+    }
     if (hc::fused_supported(hc, d, di)) {
         return from_cuda(hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
                                           hc_base, mixes, pre, post, comb, y, di, s));

@@ -1,0 +1,389 @@
+// hc_decode.cu -- RMS statistic + mix projection + split/Sinkhorn + collapse
+// for a few tokens (decode), hc = 4, on sm_103a ("Mix projection" page:
+// formula for m, Block.hc_mixes, Block.hc_pre; "Reading weights" page:
+// hc_split_sinkhorn).
+//
+// Work decomposition
+//   * A cluster of 16 CTAs (one per SM) takes up to 16 consecutive tokens,
+//     and one launch holds as many clusters as the device co-schedules: 64
+//     tokens run on 7 clusters (112 SMs) instead of one.
+//   * CTA r of a cluster owns channels [r*w, (r+1)*w) of every copy
+//     (w = d/16) and keeps its slice of W_mix (fp32, 24 x 4w) and of its
+//     tokens' x (bf16, tokens x 4w) in shared memory.
+//   * Partial mix numbers and sums of squares on CUDA cores: warp (g, h)
+//     takes tokens 4g..4g+3 and mixes 6h..6h+5 over all 4w features, each
+//     lane the feature pairs 64 apart starting at 2*lane; the 32 lanes'
+//     partials are then summed in lane order through shared memory.
+//   * Each CTA sends its 25 partial numbers per token (24 mixes, sum of
+//     squares) to the token's owner, CTA t of the cluster for its token t,
+//     with asynchronous 4-byte stores whose bytes complete the owner's
+//     barrier.  The owner sums the 16 records in CTA order, forms r, m and
+//     pre, sends pre to all 16 CTAs the same way and then runs the Sinkhorn
+//     for comb.
+//   * Every CTA collapses its own w channels of the cluster's tokens from the
+//     x slice it holds, so x is read from memory once.
+//
+// Every wait is bounded: a wait that exceeds the time limit sets the CTA's
+// abort flag and bit 0 of the device error word, and the CTA runs to the
+// teardown (no trap; no CTA leaves its cluster while another may still
+// address its shared memory).
+#include <cuda.h>
+
+#include <mutex>
+
+#include "hc_common.cuh"
+#include "hc_decode.h"
+#include "hc_ptx.cuh"
+
+namespace hc {
+namespace {
+
+using namespace ptx;
+
+constexpr int kCluster = 16;
+constexpr int kMix = 24;
+constexpr int kMaxTok = 16;           // tokens per cluster, one owner CTA each
+constexpr int kRecVals = kMix + 1;    // per (sender, token): 24 mixes + sum of squares
+constexpr int kRecStride = 28;        // floats between two senders' records
+constexpr int kWarps = 16;            // warp (g, h): tokens 4g.., mixes 6h..
+constexpr int kThreads = kWarps * 32;
+constexpr int kPartVals = 28;         // per warp: 4 tokens x 6 mixes + 4 sums of squares
+constexpr int kPartStride = 33;       // lanes per partial value, padded: no bank conflicts
+constexpr int kMaxW = 320;            // channels per CTA (d <= 5120)
+
+struct DecodeParams {
+    int n;
+    int d;
+    int w;     // channels per CTA, d / 16
+    int tpc;   // tokens per cluster
+    int iters;
+    int mixes_only;
+    float eps;
+    float norm_eps;
+    float F;
+    const uint16_t *x;
+    const float *w_mix;
+    const float *scale;
+    const float *base;
+    float *mixes;
+    float *pre;
+    float *post;
+    float *comb;
+    uint16_t *y;
+    unsigned int *err;
+};
+
+__host__ __device__ constexpr int round4(int t) { return (t + 3) & ~3; }
+
+// W slice, later reused for the lanes' partials
+__host__ __device__ constexpr size_t wreg_bytes(int w) {
+    return (size_t)kMix * 4 * w * 4 > (size_t)kWarps * kPartVals * kPartStride * 4
+               ? (size_t)kMix * 4 * w * 4
+               : (size_t)kWarps * kPartVals * kPartStride * 4;
+}
+__host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
+    return (size_t)round4(tpc) * 4 * w * 2;
+}
+__host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
+    return wreg_bytes(w) + xreg_bytes(w, tpc) + kCluster * kRecStride * 4 + kMaxTok * 4 * 4 +
+           2 * 8 + 16;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int w = p.w, nf = 4 * w;
+    const size_t wreg = wreg_bytes(w);
+    float *ws = reinterpret_cast<float *>(smem);    // [24][nf]
+    float *part = ws;                               // [16 warps][28][33], after the projection
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem + wreg);  // [round4(tpc)][nf]
+    float *recv = reinterpret_cast<float *>(smem + wreg + xreg_bytes(w, p.tpc));  // [16][28]
+    float *preb = recv + kCluster * kRecStride;     // [16][4]: pre of the cluster's tokens
+    uint64_t *bars = reinterpret_cast<uint64_t *>(preb + kMaxTok * 4);
+    int *abort_word = reinterpret_cast<int *>(bars + 2);
+    volatile int *abort = abort_word;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)(blockIdx.x % kCluster);
+    const int64_t tok0 = (int64_t)(blockIdx.x / kCluster) * p.tpc;
+    const int tv = (int)((int64_t)p.n - tok0 < p.tpc ? (int64_t)p.n - tok0 : p.tpc);
+    const bool mixes_only = p.mixes_only != 0;
+    const uint32_t bRecv = su32(bars), bPre = su32(bars + 1);
+    const int64_t F = 4LL * p.d;
+
+    // Each barrier completes once: recv when the 16 records of this CTA's
+    // token are in (owners only), pre when pre of all tv tokens is in.
+    if (threadIdx.x == 0) {
+        *abort_word = 0;
+        mbar_init(bRecv, 1);
+        mbar_init(bPre, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        if (rank < tv) mbar_expect_tx(bRecv, kCluster * kRecVals * 4);
+        if (!mixes_only) mbar_expect_tx(bPre, (uint32_t)tv * 16);
+    }
+    cluster_arrive();  // waited for before the first remote store
+
+    // W slice: row i, copy j -> W[i][j*d + r*w ...], w floats
+    {
+        const int wv = w / 4;
+        for (int idx = threadIdx.x; idx < kMix * 4 * wv; idx += kThreads) {
+            const int q = idx % wv, ij = idx / wv, j = ij % 4, i = ij / 4;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(
+                                       p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w) +
+                                   q);
+            reinterpret_cast<float4 *>(ws + i * nf + j * w)[q] = v;
+        }
+        // x slice: token t, copy j -> x[tok0+t][j][r*w ...]; rows up to the
+        // next multiple of 4 tokens are zero
+        const int xv = w / 8, tz = round4(tv);
+        for (int idx = threadIdx.x; idx < tz * 4 * xv; idx += kThreads) {
+            const int q = idx % xv, tj = idx / xv, j = tj % 4, t = tj / 4;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t < tv)
+                v = __ldg(reinterpret_cast<const uint4 *>(
+                              p.x + ((tok0 + t) * 4 + j) * (int64_t)p.d + rank * w) +
+                          q);
+            reinterpret_cast<uint4 *>(xs + t * nf + j * w)[q] = v;
+        }
+    }
+    __syncthreads();
+
+    // Partial mix numbers (and sums of squares, h == 0) of tokens 4g..4g+3.
+    const int g = warp >> 2, h = warp & 3;
+    const bool active = 4 * g < tv;
+    float acc[4][6], ssq[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        ssq[u] = 0.f;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) acc[u][k] = 0.f;
+    }
+    if (active) {
+        for (int f = 2 * lane; f < nf; f += 64) {
+            float2 wv[6];
+#pragma unroll
+            for (int k = 0; k < 6; ++k)
+                wv[k] = *reinterpret_cast<const float2 *>(ws + (6 * h + k) * nf + f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t xx = *reinterpret_cast<const uint32_t *>(xs + (4 * g + u) * nf + f);
+                const float x0 = bf16lo(xx), x1 = bf16hi(xx);
+#pragma unroll
+                for (int k = 0; k < 6; ++k) {
+                    acc[u][k] = fmaf(x0, wv[k].x, acc[u][k]);
+                    acc[u][k] = fmaf(x1, wv[k].y, acc[u][k]);
+                }
+                if (h == 0) {
+                    ssq[u] = fmaf(x0, x0, ssq[u]);
+                    ssq[u] = fmaf(x1, x1, ssq[u]);
+                }
+            }
+        }
+    }
+    __syncthreads();  // W is no longer read: its space takes the partials
+    if (active) {
+        float *pw = part + warp * kPartVals * kPartStride;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int k = 0; k < 6; ++k) pw[(u * 6 + k) * kPartStride + lane] = acc[u][k];
+            pw[(24 + u) * kPartStride + lane] = ssq[u];
+        }
+    }
+    __syncthreads();
+    cluster_wait();  // every CTA's barriers exist and are armed
+
+    // Sum each value over the 32 lanes in lane order and send it to the
+    // owner of its token: record slot [rank][mix] (slot 24: sum of squares).
+    for (int e = threadIdx.x; e < kWarps * kPartVals; e += kThreads) {
+        const int ww = e / kPartVals, v = e % kPartVals;
+        const int hh = ww & 3;
+        const int u = v < 24 ? v / 6 : v - 24;
+        const int t = 4 * (ww >> 2) + u;
+        if (t >= tv || (v >= 24 && hh != 0)) continue;
+        const int slot = v < 24 ? 6 * hh + v % 6 : kMix;
+        const float *src = part + (ww * kPartVals + v) * kPartStride;
+        float s = 0.f;
+#pragma unroll 8
+        for (int l = 0; l < 32; ++l) s += src[l];
+        st_async_f32(mapa(su32(recv + rank * kRecStride + slot), (uint32_t)t), s,
+                     mapa(bRecv, (uint32_t)t));
+    }
+
+    if (rank < tv && warp == 0) {
+        // Owner of token tok0 + rank: lane k < 25 sums value k of the 16
+        // records in CTA order.
+        if (__all_sync(0xFFFFFFFFu, wait_bar<true>(bRecv, 0, abort, p.err))) {
+            float v = 0.f;
+            if (lane < kRecVals)
+                for (int s2 = 0; s2 < kCluster; ++s2) v += recv[s2 * kRecStride + lane];
+            const float ssum = __shfl_sync(0xFFFFFFFFu, v, kMix);
+            const float r = rsqrtf(ssum / p.F + p.norm_eps);
+            const float m = v * r;
+            const int64_t t = tok0 + rank;
+            if (p.mixes != nullptr && lane < kMix) p.mixes[t * kMix + lane] = m;
+            if (!mixes_only) {
+                float mm[kMix], bse[kMix];
+#pragma unroll
+                for (int k = 0; k < kMix; ++k) {
+                    mm[k] = __shfl_sync(0xFFFFFFFFu, m, k);
+                    bse[k] = __ldg(p.base + k);
+                }
+                const float s0 = __ldg(p.scale + 0), s1 = __ldg(p.scale + 1),
+                            s2 = __ldg(p.scale + 2);
+                float pr[4], po[4];
+                split_pre_post<4>([&](int k) { return mm[k]; }, [&](int k) { return bse[k]; },
+                                  s0, s1, p.eps, pr, po);
+                // pre to every CTA of the cluster, then comb off the collapse's path
+                if (lane < kCluster)
+                    st_async_v4(mapa(su32(preb + rank * 4), (uint32_t)lane), pr[0], pr[1], pr[2],
+                                pr[3], mapa(bPre, (uint32_t)lane));
+                if (lane == 0) {
+                    float Cm[4][4];
+                    sinkhorn_comb<4>([&](int k) { return mm[k]; },
+                                     [&](int k) { return bse[k]; }, s2, p.iters, p.eps, Cm);
+                    reinterpret_cast<float4 *>(p.pre)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+                    reinterpret_cast<float4 *>(p.post)[t] =
+                        make_float4(po[0], po[1], po[2], po[3]);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
+                            make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
+                }
+            }
+        }
+    } else if (!mixes_only && warp > 0) {
+        // Collapse y = sum_j pre_j x_j of this CTA's channels, warps 1..15.
+        if (__all_sync(0xFFFFFFFFu, wait_bar<true>(bPre, 0, abort, p.err))) {
+            const int xv = w / 8;
+            for (int o = threadIdx.x - 32; o < tv * xv; o += kThreads - 32) {
+                const int t = o / xv, q = o % xv;
+                const float4 pr = reinterpret_cast<const float4 *>(preb)[t];
+                const uint16_t *xt = xs + t * nf;
+                float acc8[8], f8[8];
+                unpack8(reinterpret_cast<const uint4 *>(xt)[q], f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc8[e] = pr.x * f8[e];
+                unpack8(reinterpret_cast<const uint4 *>(xt + w)[q], f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.y, f8[e], acc8[e]);
+                unpack8(reinterpret_cast<const uint4 *>(xt + 2 * w)[q], f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.z, f8[e], acc8[e]);
+                unpack8(reinterpret_cast<const uint4 *>(xt + 3 * w)[q], f8);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.w, f8[e], acc8[e]);
+                st_stream(reinterpret_cast<uint4 *>(p.y + (tok0 + t) * (int64_t)p.d + rank * w) +
+                              q,
+                          pack8(acc8));
+            }
+        }
+    }
+
+    // A CTA that took a store from another CTA waited for it above, so no
+    // store is still in flight toward a CTA that passes this barrier.
+    __syncwarp();
+    __syncthreads();
+    cluster_sync_all();
+}
+
+// ---------------------------------------------------------------- host
+
+struct DevState {
+    bool init = false;
+    bool ok = false;
+    int max_clusters = 0;
+};
+std::mutex g_dmu;
+DevState g_dec[64];
+
+const DevState &dec_state(const DeviceInfo &di) {
+    std::lock_guard<std::mutex> lk(g_dmu);
+    DevState &st = g_dec[di.device];
+    if (st.init) return st;
+    st.init = true;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
+    if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
+    const size_t smem = smem_bytes(kMaxW, kMaxTok);
+    if (cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_decode, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
+        cudaGetLastError();
+        return st;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kCluster);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kCluster;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, k_decode, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return st;
+    }
+    st.max_clusters = nc;
+    st.ok = nc > 0;
+    return st;
+}
+
+}  // namespace
+
+bool decode_supported(int64_t n, int hc, int64_t d, const DeviceInfo &di) {
+    if (hc != 4 || n < 1 || d % (kCluster * 16) != 0 || d > (int64_t)kCluster * kMaxW) return false;
+    if (forced_path() != kPathAuto) return false;
+    const DevState &st = dec_state(di);
+    return st.ok && n <= (int64_t)kMaxTok * st.max_clusters;
+}
+
+cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                          const uint16_t *x, const float *w, const float *scale,
+                          const float *base, float *mixes, float *pre, float *post,
+                          float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+    const DevState &st = dec_state(di);
+    if (!st.ok || hc != 4 || n < 1 || n > (int64_t)kMaxTok * st.max_clusters)
+        return cudaErrorNotSupported;
+    DecodeParams p;
+    p.n = (int)n;
+    p.d = (int)d;
+    p.w = (int)(d / kCluster);
+    p.tpc = (int)((n + st.max_clusters - 1) / st.max_clusters);
+    p.iters = iters;
+    p.mixes_only = pre == nullptr ? 1 : 0;
+    p.eps = eps;
+    p.norm_eps = norm_eps;
+    p.F = (float)(4 * d);
+    p.x = x;
+    p.w_mix = w;
+    p.scale = scale;
+    p.base = base;
+    p.mixes = mixes;
+    p.pre = pre;
+    p.post = post;
+    p.comb = comb;
+    p.y = y;
+    p.err = di.err_word;
+    const int nclusters = (int)((n + p.tpc - 1) / p.tpc);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes(p.w, p.tpc);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = kCluster;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode, p);
+    if (e != cudaSuccess) return e;
+    return launched();
+}
+
+}  // namespace hc

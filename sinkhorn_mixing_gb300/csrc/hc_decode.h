@@ -1,0 +1,25 @@
+// hc_decode.h -- the few-token (decode) path behind hc_mixes_pre and
+// hc_mixes: one launch spreads up to 16 tokens per 16-CTA cluster over every
+// cluster the device holds.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hc_internal.h"
+
+namespace hc {
+
+// True when the decode kernel handles n tokens of this (hc, d) on the
+// current device.
+bool decode_supported(int64_t n, int hc, int64_t d, const DeviceInfo &di);
+
+// pre == nullptr selects the projection-only mode (hc_mixes): only `mixes`
+// is written.  Otherwise pre, post, comb and y are written, and mixes when
+// it is not null.
+cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                          const uint16_t *x, const float *w, const float *scale,
+                          const float *base, float *mixes, float *pre, float *post,
+                          float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s);
+
+}  // namespace hc

@@ -44,9 +44,12 @@
 
 #include "hc_common.cuh"
 #include "hc_fused.h"
+#include "hc_ptx.cuh"
 
 namespace hc {
 namespace {
+
+using namespace ptx;
 
 constexpr int kCluster = 16;             // CTAs per cluster
 constexpr int kTM = 64;                  // tokens per tile
@@ -62,7 +65,6 @@ constexpr int kRec = 28;                 // floats per partial record (24 + ssq 
 constexpr uint32_t kRecvTx = kCluster * kOwn * 7 * 16;
 constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
-constexpr uint64_t kTimeoutNs = 1000000000ull;  // 1 s
 // The producer runs at most kLag tiles ahead of this CTA's collapse, which
 // re-reads every tile from L2 and so needs it to still be there.
 constexpr int kLag = 3;
@@ -108,107 +110,6 @@ struct FusedParams {
     uint16_t *y;
     unsigned int *err;
 };
-
-// ------------------------------------------------------------ PTX helpers
-
-__device__ __forceinline__ uint32_t su32(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ uint64_t gtimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar, uint32_t count = 1) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count)
-                 : "memory");
-}
-
-// Arrive on a barrier of another CTA of the cluster (address from mapa),
-// without release ordering: a cluster-scope release waits for the memory
-// traffic still in flight, which costs microseconds on a streaming SM.  Used
-// only where every access the arrive must follow has already completed.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
-                     cluster_addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase of `bar` with the given parity.  Returns false
-// (and raises the abort flag) on timeout or when the CTA is already aborting.
-template <bool kClusterScope>
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort,
-                                         unsigned int *err) {
-    if (kClusterScope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    const uint64_t t0 = gtimer();
-    while (true) {
-        if (kClusterScope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-        if (*abort) return false;
-        if (gtimer() - t0 > kTimeoutNs) {
-            *abort = 1;
-            atomicOr(err, kErrWaitTimeout);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// Asynchronous 16-byte store into another CTA's shared memory; its bytes
-// complete a transaction count on the destination CTA's barrier `bar`.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d,
-                                            uint32_t bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-        "[%5];" ::"r"(addr),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, int c3, uint32_t bar) {
@@ -826,17 +727,13 @@ const DevState &dev_state(const DeviceInfo &di) {
     return st;
 }
 
-bool path_forced_general() {
-    const char *e = getenv("HCMIX_PATH");
-    return e != nullptr && e[0] == 'g';
-}
 
 }  // namespace
 
 bool fused_supported(int hc, int64_t d, const DeviceInfo &di) {
     if (hc != 4 || d % (kCluster * 64) != 0 || d < kCluster * 64 || d > kMaxNcc * kCluster * 64)
         return false;
-    if (path_forced_general()) return false;
+    if (forced_path() == kPathGeneral) return false;
     return dev_state(di).ok;
 }
 

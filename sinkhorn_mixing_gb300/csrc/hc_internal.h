@@ -16,6 +16,12 @@ struct DeviceInfo {
 // Current device's SM count and error-word address (cached per device).
 cudaError_t device_info(DeviceInfo *out);
 
+// Path override for tests and diagnosis, read from the environment at each
+// call: HCMIX_PATH=general forces the three-kernel path, HCMIX_PATH=fused
+// skips the decode kernel; unset (or anything else) chooses by shape.
+enum ForcedPath { kPathAuto = 0, kPathGeneral = 1, kPathFused = 2 };
+ForcedPath forced_path();
+
 // Adds k to the process-wide count of enqueued kernels (hc_launch_count).
 void count_launches(int k);
 

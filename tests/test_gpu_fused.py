@@ -15,6 +15,18 @@ from sinkhorn_mixing_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def fused_path_only():
+    """Small token counts would otherwise take the decode kernel."""
+    old = os.environ.get("HCMIX_PATH")
+    os.environ["HCMIX_PATH"] = "fused"
+    yield
+    if old is None:
+        os.environ.pop("HCMIX_PATH", None)
+    else:
+        os.environ["HCMIX_PATH"] = old
+
+
 @pytest.fixture(scope="module")
 def hc():
     from sinkhorn_mixing_gb300 import build
@@ -102,7 +114,7 @@ def test_fused_agrees_with_general_path(hc):
         torch.cuda.synchronize()
         assert hc.hc_launch_count() - before == 3
     finally:
-        del os.environ["HCMIX_PATH"]
+        os.environ["HCMIX_PATH"] = "fused"
     ya, pa, qa, ca, ma = a
     yb, pb, qb, cb, mb = b
     torch.testing.assert_close(ma, mb, rtol=1e-4, atol=1e-4)
