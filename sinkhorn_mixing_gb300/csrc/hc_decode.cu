@@ -8,12 +8,15 @@
 //     and one launch holds as many clusters as the device co-schedules: 64
 //     tokens run on 7 clusters (112 SMs) instead of one.
 //   * CTA r of a cluster owns channels [r*w, (r+1)*w) of every copy
-//     (w = d/16) and keeps its slice of W_mix (fp32, 24 x 4w) and of its
-//     tokens' x (bf16, tokens x 4w) in shared memory.
-//   * Partial mix numbers and sums of squares on CUDA cores: warp (g, h)
-//     takes tokens 4g..4g+3 and mixes 6h..6h+5 over all 4w features, each
-//     lane the feature pairs 64 apart starting at 2*lane; the 32 lanes'
-//     partials are then summed in lane order through shared memory.
+//     (w = d/16) and keeps its slice of W_mix (fp32, 24 x 4 x w) and of its
+//     tokens' x (bf16, tokens x 4 x w) in shared memory.
+//   * The slices arrive by asynchronous copies, one group per copy j; the
+//     projection of copy j starts when its group is in.
+//   * Partial mix numbers and sums of squares on CUDA cores (packed
+//     two-wide fma): warp (g, h) takes tokens 4g..4g+3 and mixes 6h..6h+5
+//     over all 4w features, each lane the feature pairs 64 apart starting at
+//     2*lane; the 32 lanes' partials are then summed in lane order through
+//     shared memory.
 //   * Each CTA sends its 25 partial numbers per token (24 mixes, sum of
 //     squares) to the token's owner, CTA t of the cluster for its token t,
 //     with asynchronous 4-byte stores whose bytes complete the owner's
@@ -75,12 +78,45 @@ struct DecodeParams {
 
 __host__ __device__ constexpr int round4(int t) { return (t + 3) & ~3; }
 
-// W slice, later reused for the lanes' partials
+// 16-byte asynchronous copy global -> shared (cached in L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most `left` of this thread's copy groups are still pending.
+__device__ __forceinline__ void cp_async_wait(int left) {
+    switch (left) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    }
+}
+
+// d += a * b on both halves of a packed pair of binary32 numbers.
+__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo + hi;
+}
+
+// W slice [24][4w] fp32, later reused for the lanes' partials
 __host__ __device__ constexpr size_t wreg_bytes(int w) {
     return (size_t)kMix * 4 * w * 4 > (size_t)kWarps * kPartVals * kPartStride * 4
                ? (size_t)kMix * 4 * w * 4
                : (size_t)kWarps * kPartVals * kPartStride * 4;
 }
+// x slice [round4(tpc)][4w] bf16
 __host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
     return (size_t)round4(tpc) * 4 * w * 2;
 }
@@ -121,60 +157,60 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     }
     cluster_arrive();  // waited for before the first remote store
 
-    // W slice: row i, copy j -> W[i][j*d + r*w ...], w floats
+    // W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) and x slice
+    // (token t, copy j -> x[tok0+t][j][r*w ...]) as asynchronous copies, one
+    // group per copy j, so that the projection of copy j starts as soon as
+    // its group is in.  Rows up to the next multiple of 4 tokens are zero.
+    // Rows by warp, 16-byte pieces by lane: no division in the index math.
     {
-        const int wv = w / 4;
-        for (int idx = threadIdx.x; idx < kMix * 4 * wv; idx += kThreads) {
-            const int q = idx % wv, ij = idx / wv, j = ij % 4, i = ij / 4;
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(
-                                       p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w) +
-                                   q);
-            reinterpret_cast<float4 *>(ws + i * nf + j * w)[q] = v;
-        }
-        // x slice: token t, copy j -> x[tok0+t][j][r*w ...]; rows up to the
-        // next multiple of 4 tokens are zero
-        const int xv = w / 8, tz = round4(tv);
-        for (int idx = threadIdx.x; idx < tz * 4 * xv; idx += kThreads) {
-            const int q = idx % xv, tj = idx / xv, j = tj % 4, t = tj / 4;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t < tv)
-                v = __ldg(reinterpret_cast<const uint4 *>(
-                              p.x + ((tok0 + t) * 4 + j) * (int64_t)p.d + rank * w) +
-                          q);
-            reinterpret_cast<uint4 *>(xs + t * nf + j * w)[q] = v;
+        const int wv = w / 4, xv = w / 8, tz = round4(tv);
+        for (int j = 0; j < 4; ++j) {
+            for (int i = warp; i < kMix; i += kWarps) {
+                const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
+                const uint32_t dst = su32(ws + i * nf + j * w);
+                for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
+            }
+            for (int t = warp; t < tz; t += kWarps) {
+                uint16_t *dst = xs + t * nf + j * w;
+                if (t < tv) {
+                    const uint16_t *src = p.x + ((tok0 + t) * 4 + j) * (int64_t)p.d + rank * w;
+                    for (int q = lane; q < xv; q += 32) cp_async16(su32(dst + 8 * q), src + 8 * q);
+                } else {
+                    for (int q = lane; q < xv; q += 32)
+                        *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            cp_async_commit();
         }
     }
-    __syncthreads();
 
-    // Partial mix numbers (and sums of squares, h == 0) of tokens 4g..4g+3.
+    // Partial mix numbers (and sums of squares, h == 0) of tokens 4g..4g+3,
+    // as pairs (even feature, odd feature) summed at the end.
     const int g = warp >> 2, h = warp & 3;
     const bool active = 4 * g < tv;
-    float acc[4][6], ssq[4];
+    uint64_t acc[4][6], ssq[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        ssq[u] = 0.f;
+        ssq[u] = 0;
 #pragma unroll
-        for (int k = 0; k < 6; ++k) acc[u][k] = 0.f;
+        for (int k = 0; k < 6; ++k) acc[u][k] = 0;
     }
-    if (active) {
-        for (int f = 2 * lane; f < nf; f += 64) {
-            float2 wv[6];
+    for (int j = 0; j < 4; ++j) {
+        cp_async_wait(3 - j);
+        __syncthreads();  // every thread's copies of group j are in
+        if (!active) continue;
+        for (int f = j * w + 2 * lane; f < (j + 1) * w; f += 64) {
+            uint64_t wv[6];
 #pragma unroll
             for (int k = 0; k < 6; ++k)
-                wv[k] = *reinterpret_cast<const float2 *>(ws + (6 * h + k) * nf + f);
+                wv[k] = *reinterpret_cast<const uint64_t *>(ws + (6 * h + k) * nf + f);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint32_t xx = *reinterpret_cast<const uint32_t *>(xs + (4 * g + u) * nf + f);
-                const float x0 = bf16lo(xx), x1 = bf16hi(xx);
+                const uint64_t xp = pack2(bf16lo(xx), bf16hi(xx));
 #pragma unroll
-                for (int k = 0; k < 6; ++k) {
-                    acc[u][k] = fmaf(x0, wv[k].x, acc[u][k]);
-                    acc[u][k] = fmaf(x1, wv[k].y, acc[u][k]);
-                }
-                if (h == 0) {
-                    ssq[u] = fmaf(x0, x0, ssq[u]);
-                    ssq[u] = fmaf(x1, x1, ssq[u]);
-                }
+                for (int k = 0; k < 6; ++k) ffma2(acc[u][k], xp, wv[k]);
+                if (h == 0) ffma2(ssq[u], xp, xp);
             }
         }
     }
@@ -184,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
 #pragma unroll
-            for (int k = 0; k < 6; ++k) pw[(u * 6 + k) * kPartStride + lane] = acc[u][k];
-            pw[(24 + u) * kPartStride + lane] = ssq[u];
+            for (int k = 0; k < 6; ++k) pw[(u * 6 + k) * kPartStride + lane] = sum2(acc[u][k]);
+            pw[(24 + u) * kPartStride + lane] = sum2(ssq[u]);
         }
     }
     __syncthreads();
@@ -254,26 +290,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         // Collapse y = sum_j pre_j x_j of this CTA's channels, warps 1..15.
         if (__all_sync(0xFFFFFFFFu, wait_bar<true>(bPre, 0, abort, p.err))) {
             const int xv = w / 8;
-            for (int o = threadIdx.x - 32; o < tv * xv; o += kThreads - 32) {
-                const int t = o / xv, q = o % xv;
+            for (int t = warp - 1; t < tv; t += kWarps - 1) {
                 const float4 pr = reinterpret_cast<const float4 *>(preb)[t];
                 const uint16_t *xt = xs + t * nf;
-                float acc8[8], f8[8];
-                unpack8(reinterpret_cast<const uint4 *>(xt)[q], f8);
+                uint4 *yt = reinterpret_cast<uint4 *>(p.y + (tok0 + t) * (int64_t)p.d + rank * w);
+                for (int q = lane; q < xv; q += 32) {
+                    float acc8[8], f8[8];
+                    unpack8(reinterpret_cast<const uint4 *>(xt)[q], f8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc8[e] = pr.x * f8[e];
-                unpack8(reinterpret_cast<const uint4 *>(xt + w)[q], f8);
+                    for (int e = 0; e < 8; ++e) acc8[e] = pr.x * f8[e];
+                    unpack8(reinterpret_cast<const uint4 *>(xt + w)[q], f8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.y, f8[e], acc8[e]);
-                unpack8(reinterpret_cast<const uint4 *>(xt + 2 * w)[q], f8);
+                    for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.y, f8[e], acc8[e]);
+                    unpack8(reinterpret_cast<const uint4 *>(xt + 2 * w)[q], f8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.z, f8[e], acc8[e]);
-                unpack8(reinterpret_cast<const uint4 *>(xt + 3 * w)[q], f8);
+                    for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.z, f8[e], acc8[e]);
+                    unpack8(reinterpret_cast<const uint4 *>(xt + 3 * w)[q], f8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.w, f8[e], acc8[e]);
-                st_stream(reinterpret_cast<uint4 *>(p.y + (tok0 + t) * (int64_t)p.d + rank * w) +
-                              q,
-                          pack8(acc8));
+                    for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.w, f8[e], acc8[e]);
+                    st_stream(yt + q, pack8(acc8));
+                }
             }
         }
     }
@@ -323,7 +359,7 @@ const DevState &dec_state(const DeviceInfo &di) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    if (cudaOccupancyMaxActiveClusters(&nc, k_decode, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&nc, (void *)k_decode, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return st;
     }

@@ -661,20 +661,6 @@ struct DevState {
 std::mutex g_fmu;
 DevState g_dev[64];
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
 using FusedKernel = void (*)(CUtensorMap, FusedParams);
 
 // The instantiation for w = 64 * ncc channels per CTA.
@@ -696,7 +682,7 @@ const DevState &dev_state(const DeviceInfo &di) {
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
-    if (encode_fn() == nullptr) return st;
+    if (tensor_map_encoder() == nullptr) return st;
     for (int ncc = 1; ncc <= kMaxNcc; ++ncc) {
         if (cudaFuncSetAttribute(kernel_for(ncc), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem_bytes(ncc)) != cudaSuccess)
@@ -753,7 +739,7 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     const cuuint64_t gstride[3] = {(cuuint64_t)(F * 2), 128, (cuuint64_t)(d * 2)};
     const cuuint32_t box[4] = {64, kTM, 1, 4};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
-    CUresult r = encode_fn()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+    CUresult r = tensor_map_encoder()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                              const_cast<uint16_t *>(x), gdim, gstride, box, estride,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

@@ -2,6 +2,8 @@
 // Arguments are already validated by hc_abi.cu when these are called.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +23,9 @@ cudaError_t device_info(DeviceInfo *out);
 // skips the decode kernel; unset (or anything else) chooses by shape.
 enum ForcedPath { kPathAuto = 0, kPathGeneral = 1, kPathFused = 2 };
 ForcedPath forced_path();
+
+// The driver's cuTensorMapEncodeTiled, or nullptr when it is unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Adds k to the process-wide count of enqueued kernels (hc_launch_count).
 void count_launches(int k);
