@@ -51,6 +51,8 @@ def parse(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the 64-token decode latency line item")
     return ap.parse_args(argv)
 
 
@@ -179,6 +181,62 @@ def traffic_record(kernel):
     if h != rec.get("source_sha256_16"):
         return None
     return rec
+
+
+def decode_latency(hc, dev, reps=20, replays=10):
+    """Latency of one decode step (hc_mixes_pre + hc_post on the 64-token
+    decode workload) replayed from a captured CUDA graph of `reps` steps, and
+    issued eagerly from Python.  Its 5.25 MB of inputs stay in L2 between
+    steps, as they would between a decode step's sublayers."""
+    import torch
+    from sinkhorn_mixing_gb300 import inputs
+    wl = inputs.WORKLOADS["decode"]
+    n, H, d = wl.n, wl.hc, wl.d
+    s = inputs.make_streams(wl, device=dev)
+    p = inputs.make_params(wl, device=dev)
+    x, out = s["x"], s["out"]
+    pre = torch.empty((n, H), device=dev)
+    post = torch.empty((n, H), device=dev)
+    comb = torch.empty((n, H, H), device=dev)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    ys = torch.empty((n, H, d), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(max(256, hc.hc_workspace_bytes(n, H, d)), dtype=torch.uint8, device=dev)
+
+    def step():
+        hc.hc_mixes_pre(x, p["w"], p["hc_scale"], p["hc_base"], wl.iters[0], wl.eps,
+                        wl.norm_eps, pre=pre, post=post, comb=comb, y=y, workspace=wsp)
+        hc.hc_post(out, x, post, comb, y=ys)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(5):
+            step()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(reps):
+                step()
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(side)
+        for _ in range(replays):
+            g.replay()
+        b.record(side)
+        torch.cuda.synchronize(dev)
+        graph_us = a.elapsed_time(b) * 1e3 / (replays * reps)
+        a.record(side)
+        for _ in range(reps * replays):
+            step()
+        b.record(side)
+        torch.cuda.synchronize(dev)
+        eager_us = a.elapsed_time(b) * 1e3 / (replays * reps)
+    return {"workload": DESCR["decode"], "us_per_step_graph": graph_us,
+            "us_per_step_eager": eager_us, "tokens_per_s_graph": n / graph_us * 1e6,
+            "l2": "warm (inputs stay in L2 between steps)",
+            "graph": "%d steps per captured graph, %d replays" % (reps, replays)}
 
 
 def cpu_baseline(wl, seconds):
@@ -394,6 +452,10 @@ def run_ours(args, wl, ws, rank, local):
         "e2e": e2e,
         "gpu_launches": int(launches),
     }
+    if not args.no_decode:
+        line["decode"] = decode_latency(hc, dev)
+        if hc.hc_device_error(clear=True):
+            raise RuntimeError("device error word set during the decode measurement")
     if ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     print(json.dumps(line), flush=True)

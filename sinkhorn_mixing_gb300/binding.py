@@ -74,9 +74,37 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# The raw handle of the current stream without building a Stream object
+# (a few microseconds per call on the decode path); public API otherwise.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(dev: torch.device, stream) -> ctypes.c_void_p:
-    s = torch.cuda.current_stream(dev) if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
+    if _raw_stream is not None:
+        return ctypes.c_void_p(_raw_stream(dev.index))
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+class _on_device:
+    """Makes `dev` the current device for the call, switching only when it
+    is not already current."""
+
+    def __init__(self, dev: torch.device):
+        self.idx = dev.index
+        self.prev = None
+
+    def __enter__(self):
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+        return False
 
 
 def _need(t: torch.Tensor, name: str, dtype, dev=None):
@@ -84,9 +112,9 @@ def _need(t: torch.Tensor, name: str, dtype, dev=None):
         raise TypeError("%s must be a torch.Tensor" % name)
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if dev is not None and t.device != dev:
+    if dev is not None and t.get_device() != dev.index:
         raise ValueError("%s is on %s, expected %s" % (name, t.device, dev))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
@@ -129,7 +157,7 @@ def hc_mixes(x, w_mix, norm_eps: float = 1e-20, mixes=None, stream=None):
     _need(w_mix, "w_mix", torch.float32, dev)
     mix = (2 + hc) * hc
     mixes = _out(mixes, "mixes", lead + (mix,), torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().hc_mixes(n, hc, d, float(norm_eps), _ptr(x), _ptr(w_mix), _ptr(mixes),
                               _stream(dev, stream)), "hc_mixes")
     return mixes
@@ -151,7 +179,7 @@ def hc_split_sinkhorn(mixes, hc_scale, hc_base, hc_mult: int = 4, sinkhorn_iters
     pre = _out(pre, "pre", lead + (hc,), torch.float32, dev)
     post = _out(post, "post", lead + (hc,), torch.float32, dev)
     comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().hc_split_sinkhorn(n, hc, int(sinkhorn_iters), float(eps), _ptr(mixes),
                                        _ptr(hc_scale), _ptr(hc_base), _ptr(pre), _ptr(post),
                                        _ptr(comb), _stream(dev, stream)), "hc_split_sinkhorn")
@@ -167,7 +195,7 @@ def hc_pre(x, pre, y=None, stream=None):
     if pre.numel() != n * hc:
         raise ValueError("pre must hold n*hc values")
     y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().hc_pre(n, hc, d, _ptr(x), _ptr(pre), _ptr(y), _stream(dev, stream)),
                "hc_pre")
     return y
@@ -187,7 +215,7 @@ def hc_post(out, residual, post, comb, y=None, stream=None):
     if post.numel() != n * hc or comb.numel() != n * hc * hc:
         raise ValueError("post/comb sizes do not match residual")
     y = _out(y, "y", lead + (hc, d), torch.bfloat16, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().hc_post(n, hc, d, _ptr(out), _ptr(residual), _ptr(post), _ptr(comb), _ptr(y),
                              _stream(dev, stream)), "hc_post")
     return y
@@ -219,7 +247,7 @@ def hc_mixes_pre(x, w_mix, hc_scale, hc_base, sinkhorn_iters: int = 20, eps: flo
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
         wbytes = workspace.numel()
-    with torch.cuda.device(dev):
+    with _on_device(dev):
         _check(lib().hc_mixes_pre(n, hc, d, int(sinkhorn_iters), float(eps), float(norm_eps),
                                   _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
                                   _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb), _ptr(y),
