@@ -2,6 +2,7 @@
 // validation, path selection and launch.  Nothing here allocates memory.
 #include <math.h>
 #include <stdlib.h>
+#include <string.h>
 #include <atomic>
 #include <mutex>
 
@@ -43,9 +44,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 ForcedPath forced_path() {
     const char *e = getenv("HCMIX_PATH");
     if (e == nullptr) return kPathAuto;
-    if (e[0] == 'g') return kPathGeneral;
-    if (e[0] == 'f') return kPathFused;
+    if (strcmp(e, "general") == 0) return kPathGeneral;
+    if (strcmp(e, "fused") == 0) return kPathFused;
+    if (strcmp(e, "ffma") == 0) return kPathFfma;
     return kPathAuto;
+}
+
+// The projection of the general path: tensor cores when they take the shape.
+cudaError_t launch_projection(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                              const float *w, float *mixes, const DeviceInfo &di,
+                              cudaStream_t s) {
+    if (mixtc_supported(hc, d, di)) return launch_mixtc(n, hc, d, norm_eps, x, w, mixes, di, s);
+    return launch_mixes(n, hc, d, norm_eps, x, w, mixes, di, s);
 }
 
 cudaError_t device_info(DeviceInfo *out) {
@@ -181,7 +191,7 @@ hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t 
                                           w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
                                           nullptr, nullptr, di, s));
     }
-    return from_cuda(hc::launch_mixes(n, hc, d, norm_eps, x, w_mix, mixes, di, s));
+    return from_cuda(hc::launch_projection(n, hc, d, norm_eps, x, w_mix, mixes, di, s));
 }
 
 hc_status hc_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,
@@ -283,7 +293,7 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float
                                           hc_base, mixes, pre, post, comb, y, di, s));
     }
     // General path: three kernels, the mix numbers passing through m.
-    cudaError_t e = hc::launch_mixes(n, hc, d, norm_eps, x, w_mix, m, di, s);
+    cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, m, di, s);
     if (e == cudaSuccess)
         e = hc::launch_split_sinkhorn(n, hc, iters, eps, m, hc_scale, hc_base, pre, post, comb,
                                       di, s);

@@ -19,9 +19,10 @@ struct DeviceInfo {
 cudaError_t device_info(DeviceInfo *out);
 
 // Path override for tests and diagnosis, read from the environment at each
-// call: HCMIX_PATH=general forces the three-kernel path, HCMIX_PATH=fused
-// skips the decode kernel; unset (or anything else) chooses by shape.
-enum ForcedPath { kPathAuto = 0, kPathGeneral = 1, kPathFused = 2 };
+// call: HCMIX_PATH=general forces the three-kernel path, HCMIX_PATH=ffma the
+// same path with the CUDA-core projection, HCMIX_PATH=fused skips the decode
+// kernel; unset (or anything else) chooses by shape.
+enum ForcedPath { kPathAuto = 0, kPathGeneral = 1, kPathFused = 2, kPathFfma = 3 };
 ForcedPath forced_path();
 
 // The driver's cuTensorMapEncodeTiled, or nullptr when it is unavailable.
@@ -38,6 +39,18 @@ inline cudaError_t launched(int k = 1) {
 }
 
 cudaError_t launch_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                         const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s);
+
+// The general path's projection: launch_mixtc when it takes the shape, else
+// launch_mixes.
+cudaError_t launch_projection(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                              const float *w, float *mixes, const DeviceInfo &di,
+                              cudaStream_t s);
+
+// Tensor-core projection with W streamed (hc_mixtc.cu): hc in {4, 8} and
+// hc*d a multiple of 64.
+bool mixtc_supported(int hc, int64_t d, const DeviceInfo &di);
+cudaError_t launch_mixtc(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
                          const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s);
 
 cudaError_t launch_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,

@@ -1,0 +1,463 @@
+// hc_mixtc.cu -- RMS statistic + mix projection on the tensor cores for any
+// token count, hc in {4, 8}, with W_mix streamed rather than resident
+// ("Mix projection" page: the formula for m, Block.hc_mixes).
+//
+// Work decomposition
+//   * Persistent CTAs, one per SM, take 128-token tiles in turn.  A tile's
+//     feature axis is walked in stages of 64 features: TMA brings the x
+//     sub-tile [128 tokens x 64] (128-byte swizzled, K-major) and the W
+//     sub-tile [mix x 64] (fp32 rows) into a ring of kStages slots.
+//   * 4 convert warps split the W sub-tile into bf16 hi rows (bf16(W)) and lo
+//     rows (bf16(W - hi)) in the swizzled K-major layout the tensor core
+//     reads, so no converted copy of W is kept in memory.
+//   * Per stage, 4 tcgen05.mma (M = 128 tokens, N = 2*mix rows of hi and lo,
+//     K = 16) accumulate x.(W_hi + W_lo) in TMEM (binary32).  bf16 x is exact
+//     and hi + lo carries ~16 mantissa bits of W.  The tensor core's own
+//     accumulation loses about one binary32 unit per step in one direction, so
+//     a tile's feature axis is cut into parts of kPart stages (256 MMA steps):
+//     each part accumulates in one of two TMEM buffers and the epilogue adds
+//     the parts in binary32 registers (round to nearest) while the MMAs go on
+//     in the other buffer.  One chain over 40,960 features was off by 1.4e-4
+//     relative.
+//   * 4 square warps add x^2 per token from the same sub-tiles.
+//   * 4 epilogue warps (one per TMEM lane quadrant, 32 tokens each) read the
+//     accumulators, add hi and lo, scale by r = 1/sqrt(mean x^2 + eps) and
+//     write the mix numbers.
+// Every wait is bounded; a timeout sets the CTA's abort flag and bit 0 of the
+// device error word, and all roles run to the teardown (no trap; TMEM and
+// in-flight copies are always waited for).
+#include <cuda.h>
+
+#include <mutex>
+
+#include "hc_common.cuh"
+#include "hc_internal.h"
+#include "hc_ptx.cuh"
+
+namespace hc {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTok = 128;                // tokens per tile (MMA M)
+constexpr int kK = 64;                   // features per stage
+constexpr int kXBytes = kTok * kK * 2;   // x sub-tile, 16 KB
+constexpr int kPart = 64;                // stages per tensor-core accumulation chain
+constexpr int kThreads = 14 * 32;
+// warp roles
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpSq0 = 2;              // 2..5: sums of squares, 32 tokens each
+constexpr int kWarpEpi0 = 8;             // 8..11: TMEM lane quadrants 0..3
+__host__ __device__ constexpr bool is_convert_warp(int w) {
+    return w == 6 || w == 7 || w == 12 || w == 13;
+}
+__host__ __device__ constexpr int convert_index(int w) { return w < 8 ? w - 6 : w - 10; }
+
+template <int HC>
+struct Cfg {
+    static constexpr int kMix = (2 + HC) * HC;      // 24 or 80
+    static constexpr int kNW = 2 * kMix;            // B rows: hi then lo
+    static constexpr int kStages = HC == 8 ? 3 : 6;
+    static constexpr int kWfBytes = kMix * kK * 4;  // fp32 W sub-tile
+    static constexpr int kWbBytes = kNW * kK * 2;   // bf16 hi/lo sub-tile
+    static constexpr int kTmemCols = HC == 8 ? 512 : 128;  // >= 2 * kNW, power of 2
+    // tcgen05 instruction descriptor: D f32, A/B bf16, K-major, N = kNW, M = 128
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       ((uint32_t)(kNW >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    static_assert(kNW % 16 == 0 && kNW <= 256, "MMA N");
+    static_assert(2 * kNW <= kTmemCols, "two accumulator buffers");
+    static_assert(kWbBytes % 1024 == 0 && kWfBytes % 1024 == 0, "swizzle atoms and TMA alignment");
+};
+
+struct MixParams {
+    int64_t n;
+    int F;
+    int nk;         // stages per tile, F / 64
+    int num_tiles;
+    float norm_eps;
+    float* mixes;
+    unsigned int *err;
+};
+
+template <int HC>
+__host__ __device__ constexpr size_t ring_bytes() {
+    return (size_t)Cfg<HC>::kStages * (kXBytes + Cfg<HC>::kWbBytes + Cfg<HC>::kWfBytes);
+}
+
+// barrier indices
+template <int HC>
+struct Bars {
+    static constexpr int S = Cfg<HC>::kStages;
+    static constexpr int full(int s) { return s; }
+    static constexpr int conv(int s) { return S + s; }
+    static constexpr int empty(int s) { return 2 * S + s; }
+    static constexpr int acc_full(int b) { return 3 * S + b; }
+    static constexpr int acc_empty(int b) { return 3 * S + 2 + b; }
+    static constexpr int sq_full(int b) { return 3 * S + 4 + b; }
+    static constexpr int sq_empty(int b) { return 3 * S + 6 + b; }
+    static constexpr int drain = 3 * S + 8;
+    static constexpr int count = drain + 1;
+};
+
+template <int HC>
+__host__ __device__ constexpr size_t smem_bytes() {
+    return 1024 /* alignment slack */ + ring_bytes<HC>() + 2 * kTok * 4 + Bars<HC>::count * 8 + 16;
+}
+
+template <int HC>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_mixtc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+            const MixParams p) {
+    using C = Cfg<HC>;
+    using B = Bars<HC>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *xr = base;                               // [S][128 x 64] bf16, swizzled
+    uint8_t *wb = xr + (size_t)S * kXBytes;           // [S][kNW x 64] bf16, swizzled
+    float *wf = reinterpret_cast<float *>(wb + (size_t)S * C::kWbBytes);  // [S][kMix][64]
+    float *sq = wf + (size_t)S * C::kMix * kK;        // [2][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sq + 2 * kTok);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B::count);
+    int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *abort = abort_word;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = (int)blockIdx.x < p.num_tiles
+                      ? (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+                      : 0;
+    auto bar = [&](int i) { return su32(bars + i); };
+
+    if (threadIdx.x == 0) {
+        *abort_word = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar(B::full(s)), 1);
+            mbar_init(bar(B::conv(s)), 4);
+            mbar_init(bar(B::empty(s)), 5);  // MMA commit + 4 square warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(B::acc_full(b)), 1);
+            mbar_init(bar(B::acc_empty(b)), 4);
+            mbar_init(bar(B::sq_full(b)), 4);
+            mbar_init(bar(B::sq_empty(b)), 4);
+        }
+        mbar_init(bar(B::drain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(tmem_slot)),
+                     "r"(C::kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kWarpProducer) {
+        if (lane == 0) {
+            int last_use[S];
+            for (int s = 0; s < S; ++s) last_use[s] = -1;
+            bool ok = true;
+            uint32_t q = 0;
+            for (int it = 0; it < T && ok; ++it) {
+                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+                for (int kc = 0; kc < p.nk; ++kc, ++q) {
+                    const int slot = (int)(q % S);
+                    const uint32_t use = q / S;
+                    if (!wait_bar<false>(bar(B::empty(slot)), (use & 1) ^ 1, abort, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(bar(B::full(slot)), (uint32_t)(kXBytes + C::kWfBytes));
+                    tma_load_2d(su32(xr + (size_t)slot * kXBytes), &tm_x, kc * kK, tile * kTok,
+                                bar(B::full(slot)));
+                    tma_load_2d(su32(wf + (size_t)slot * C::kMix * kK), &tm_w, kc * kK, 0,
+                                bar(B::full(slot)));
+                    last_use[slot] = (int)use;
+                }
+            }
+            // no TMA may still be writing this CTA's shared memory at exit
+            for (int s = 0; s < S; ++s)
+                if (last_use[s] >= 0)
+                    wait_bar<false>(bar(B::full(s)), (uint32_t)last_use[s] & 1, abort, p.err);
+        }
+    } else if (warp == kWarpMma) {
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t q = 0, gp = 0;  // stage and accumulation-part counters
+            for (int it = 0; it < T && ok; ++it) {
+                for (int k0 = 0; k0 < p.nk && ok; k0 += kPart, ++gp) {
+                    const int b = (int)(gp & 1);
+                    if (!wait_bar<false>(bar(B::acc_empty(b)), ((gp >> 1) & 1) ^ 1, abort, p.err))
+                        break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + (uint32_t)(b * C::kNW);
+                    const int k1 = k0 + kPart < p.nk ? k0 + kPart : p.nk;
+                    for (int kc = k0; kc < k1; ++kc, ++q) {
+                        const int slot = (int)(q % S);
+                        const uint32_t par = (q / S) & 1;
+                        if (!wait_bar<false>(bar(B::full(slot)), par, abort, p.err) ||
+                            !wait_bar<false>(bar(B::conv(slot)), par, abort, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = su32(xr + (size_t)slot * kXBytes);
+                        const uint32_t b0 = su32(wb + (size_t)slot * C::kWbBytes);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                     C::kIdesc, ((kc - k0) | k) != 0);
+                        mma_commit(bar(B::empty(slot)));
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(B::acc_full(b)));
+                }
+            }
+            // all issued MMAs complete before TMEM is freed
+            mma_commit(bar(B::drain));
+            wait_bar<false>(bar(B::drain), 0, abort, p.err);
+        }
+    } else if (is_convert_warp(warp)) {
+        // W sub-tile (fp32 rows of 64) -> bf16 hi rows 0..kMix-1 and lo rows
+        // kMix..2kMix-1, 8 features per 16-byte chunk, swizzled K-major.
+        const int ci = convert_index(warp) * 32 + lane;
+        uint32_t q = 0;
+        bool ok = true;
+        for (int it = 0; it < T && ok; ++it) {
+            for (int kc = 0; kc < p.nk; ++kc, ++q) {
+                const int slot = (int)(q % S);
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::full(slot)), (q / S) & 1,
+                                                             abort, p.err))) {
+                    ok = false;
+                    break;
+                }
+                const float *src = wf + (size_t)slot * C::kMix * kK;
+                uint8_t *dst = wb + (size_t)slot * C::kWbBytes;
+                for (int e = ci; e < C::kMix * 8; e += 128) {
+                    const int i = e >> 3, c = e & 7;
+                    const float4 a = *reinterpret_cast<const float4 *>(src + i * kK + 8 * c);
+                    const float4 b2 = *reinterpret_cast<const float4 *>(src + i * kK + 8 * c + 4);
+                    float v[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w}, lo[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        lo[u] = v[u] - __bfloat162float(__float2bfloat16_rn(v[u]));
+                    uint4 hv, lv;
+                    hv.x = pack_bf16x2(v[0], v[1]);
+                    hv.y = pack_bf16x2(v[2], v[3]);
+                    hv.z = pack_bf16x2(v[4], v[5]);
+                    hv.w = pack_bf16x2(v[6], v[7]);
+                    lv.x = pack_bf16x2(lo[0], lo[1]);
+                    lv.y = pack_bf16x2(lo[2], lo[3]);
+                    lv.z = pack_bf16x2(lo[4], lo[5]);
+                    lv.w = pack_bf16x2(lo[6], lo[7]);
+                    const int rl = C::kMix + i;
+                    *reinterpret_cast<uint4 *>(dst + (i >> 3) * 1024 + (i & 7) * 128 +
+                                               ((c ^ (i & 7)) << 4)) = hv;
+                    *reinterpret_cast<uint4 *>(dst + (rl >> 3) * 1024 + (rl & 7) * 128 +
+                                               ((c ^ (rl & 7)) << 4)) = lv;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B::conv(slot)));
+            }
+        }
+    } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
+        // Sums of squares: warp 2+g takes tokens 32g..32g+31, lane = token,
+        // chunks in swizzle order so 8 consecutive lanes hit 8 bank groups.
+        const int i = 32 * (warp - kWarpSq0) + lane;
+        uint32_t q = 0;
+        bool ok = true;
+        for (int it = 0; it < T && ok; ++it) {
+            const int b = it & 1;
+            const uint32_t use = (uint32_t)(it >> 1);
+            float ss = 0.f;
+            for (int kc = 0; kc < p.nk; ++kc, ++q) {
+                const int slot = (int)(q % S);
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::full(slot)), (q / S) & 1,
+                                                             abort, p.err))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t row = su32(xr + (size_t)slot * kXBytes) + (i >> 3) * 1024 + (i & 7) * 128;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    float f[8];
+                    unpack8(lds128(row + ((m ^ (i & 7)) << 4)), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B::empty(slot)));
+            }
+            if (!ok) break;
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait_bar<false>(bar(B::sq_empty(b)), (use & 1) ^ 1, abort, p.err)))
+                break;
+            sq[b * kTok + i] = ss;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B::sq_full(b)));
+        }
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+        // TMEM lanes 32*(warp % 4).. = tokens of the tile; the parts of a
+        // tile are added in registers, then scaled by r and written.
+        const int i = 32 * (warp & 3) + lane;
+        const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
+        uint32_t gp = 0;
+        bool ok = true;
+        for (int it = 0; it < T && ok; ++it) {
+            const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+            float m[C::kMix];
+#pragma unroll
+            for (int k = 0; k < C::kMix; ++k) m[k] = 0.f;
+            for (int k0 = 0; k0 < p.nk; k0 += kPart, ++gp) {
+                const int b = (int)(gp & 1);
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::acc_full(b)), (gp >> 1) & 1,
+                                                             abort, p.err))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + tlane + (uint32_t)(b * C::kNW);
+#pragma unroll
+                for (int g = 0; g < C::kMix / 8; ++g) {
+                    float hi[8], lo[8];
+                    tmem_ld8(taddr + 8 * g, hi);
+                    tmem_ld8(taddr + C::kMix + 8 * g, lo);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) m[8 * g + e] += hi[e] + lo[e];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B::acc_empty(b)));
+            }
+            if (!ok) break;
+            const uint32_t use = (uint32_t)(it >> 1);
+            const int bs = it & 1;
+            if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::sq_full(bs)), use & 1, abort, p.err)))
+                break;
+            const float r = rsqrtf(sq[bs * kTok + i] / (float)p.F + p.norm_eps);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B::sq_empty(bs)));
+            const int64_t t = (int64_t)tile * kTok + i;
+            if (t < p.n) {
+                float4 *dst = reinterpret_cast<float4 *>(p.mixes + t * C::kMix);
+#pragma unroll
+                for (int v = 0; v < C::kMix / 4; ++v)
+                    dst[v] = make_float4(m[4 * v] * r, m[4 * v + 1] * r, m[4 * v + 2] * r,
+                                         m[4 * v + 3] * r);
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kWarpMma) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(C::kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host
+
+struct DevState {
+    bool init = false;
+    bool ok = false;
+};
+std::mutex g_mmu;
+DevState g_mix[64];
+
+template <int HC>
+bool set_attrs() {
+    return cudaFuncSetAttribute(k_mixtc<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<HC>()) == cudaSuccess;
+}
+
+const DevState &mix_state(const DeviceInfo &di) {
+    std::lock_guard<std::mutex> lk(g_mmu);
+    DevState &st = g_mix[di.device];
+    if (st.init) return st;
+    st.init = true;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
+    if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
+    if (tensor_map_encoder() == nullptr) return st;
+    if (!set_attrs<4>() || !set_attrs<8>()) {
+        cudaGetLastError();
+        return st;
+    }
+    st.ok = true;
+    return st;
+}
+
+template <int HC>
+cudaError_t launch(int64_t n, int64_t d, float norm_eps, const uint16_t *x, const float *w,
+                   float *mixes, const DeviceInfo &di, cudaStream_t s) {
+    constexpr int MIX = (2 + HC) * HC;
+    const int64_t F = (int64_t)HC * d;
+    CUtensorMap tm_x, tm_w;
+    {
+        // x as [n rows][F] bf16; one box = 64 features of 128 tokens, swizzled
+        const cuuint64_t gdim[2] = {(cuuint64_t)F, (cuuint64_t)n};
+        const cuuint64_t gstride[1] = {(cuuint64_t)F * 2};
+        const cuuint32_t box[2] = {kK, kTok};
+        const cuuint32_t es[2] = {1, 1};
+        if (tensor_map_encoder()(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t *>(x), gdim, gstride, box, es,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // W as [mix rows][F] fp32; one box = 64 features of every row
+        const cuuint64_t gdim[2] = {(cuuint64_t)F, (cuuint64_t)MIX};
+        const cuuint64_t gstride[1] = {(cuuint64_t)F * 4};
+        const cuuint32_t box[2] = {kK, (cuuint32_t)MIX};
+        const cuuint32_t es[2] = {1, 1};
+        if (tensor_map_encoder()(&tm_w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                                 const_cast<float *>(w), gdim, gstride, box, es,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    MixParams p;
+    p.n = n;
+    p.F = (int)F;
+    p.nk = (int)(F / kK);
+    p.num_tiles = (int)((n + kTok - 1) / kTok);
+    p.norm_eps = norm_eps;
+    p.mixes = mixes;
+    p.err = di.err_word;
+    const int grid = p.num_tiles < di.sms ? p.num_tiles : di.sms;
+    k_mixtc<HC><<<grid, kThreads, smem_bytes<HC>(), s>>>(tm_x, tm_w, p);
+    return launched();
+}
+
+}  // namespace
+
+bool mixtc_supported(int hc, int64_t d, const DeviceInfo &di) {
+    if (hc != 4 && hc != 8) return false;
+    if (((int64_t)hc * d) % kK != 0 || (int64_t)hc * d > (int64_t)1 << 30) return false;
+    if (forced_path() == kPathFfma) return false;
+    return mix_state(di).ok;
+}
+
+cudaError_t launch_mixtc(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
+                         const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s) {
+    if (!mix_state(di).ok || n < 1 || n >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
+    return hc == 4 ? launch<4>(n, d, norm_eps, x, w, mixes, di, s)
+                   : launch<8>(n, d, norm_eps, x, w, mixes, di, s);
+}
+
+}  // namespace hc

@@ -1,0 +1,104 @@
+"""The tensor-core projection with W streamed (the general path's projection
+for hc in {4, 8}): it matches the oracle on one tile, ragged tiles and several
+tiles per CTA, and it agrees with the CUDA-core projection."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import compare
+from sinkhorn_mixing_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def hc():
+    from sinkhorn_mixing_gb300 import build
+    build.build()
+    import sinkhorn_mixing_gb300 as m
+    m.hc_device_error(clear=True)
+    yield m
+    torch.cuda.synchronize()
+    assert m.hc_device_error(clear=True) == 0
+
+
+@pytest.fixture
+def path():
+    old = os.environ.get("HCMIX_PATH")
+
+    def set_path(v):
+        if v is None:
+            os.environ.pop("HCMIX_PATH", None)
+        else:
+            os.environ["HCMIX_PATH"] = v
+    yield set_path
+    set_path(old)
+
+
+def case(n, H, d, seed, scale_lo=0.1, scale_hi=10.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    x = torch.randn((n, H, d), device="cuda", generator=g)
+    s = torch.exp(torch.empty((n, 1, 1), device="cuda").uniform_(
+        np.log(scale_lo), np.log(scale_hi), generator=g))
+    x = (x * s).to(torch.bfloat16)
+    mix = (2 + H) * H
+    w = torch.randn((mix, H * d), device="cuda", generator=g) / (H * d) ** 0.5
+    return x, w
+
+
+def np64(t):
+    return t.detach().cpu().double().numpy()
+
+
+@pytest.mark.parametrize("H,n,d", [(8, 1, 5120), (8, 300, 5120), (8, 129, 1024),
+                                   (4, 200, 2048), (4, 5, 64), (4, 1000, 5120),
+                                   (8, 40000, 256)])
+def test_projection_matches_oracle(hc, path, H, n, d):
+    path("general")
+    x, w = case(n, H, d, 7 * n + d + H)
+    m = torch.empty((n, (2 + H) * H), device="cuda")
+    before = hc.hc_launch_count()
+    hc.hc_mixes(x, w, mixes=m)
+    torch.cuda.synchronize()
+    assert hc.hc_launch_count() - before == 1
+    idx = np.arange(n) if n <= 1200 else np.unique(np.concatenate(
+        [np.arange(8), np.arange(n - 8, n), np.random.default_rng(1).integers(0, n, 300)]))
+    compare.check_mixes(np64(m)[idx], oracle.hc_mixes(inputs.bf16_bits(x[idx]),
+                                                      w.cpu().numpy()))
+
+
+@pytest.mark.parametrize("H,n,d", [(8, 500, 5120), (4, 333, 2048)])
+def test_projection_agrees_with_cuda_core_projection(hc, path, H, n, d):
+    x, w = case(n, H, d, 3 + H)
+    path("general")
+    a = hc.hc_mixes(x, w)
+    path("ffma")
+    b = hc.hc_mixes(x, w)
+    torch.cuda.synchronize()
+    compare.check_mixes(np64(a), np64(b))
+
+
+def test_hc8_mixes_pre_through_tensor_projection(hc, path):
+    # hc = 8, stress-like logits: the three-kernel path with the tensor-core
+    # projection, checked stage by stage against the oracle
+    n, H, d = 257, 8, 5120
+    x, w = case(n, H, d, 99, 1e-3, 1e3)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    sc = torch.rand(3, device="cuda", generator=g) * 6 + 2
+    base = torch.randn(80, device="cuda", generator=g) * 5 ** 0.5
+    before = hc.hc_launch_count()
+    y, pre, post, comb, m = hc.hc_mixes_pre(x, w, sc, base, 20, want_mixes=True)
+    torch.cuda.synchronize()
+    assert hc.hc_launch_count() - before == 3
+    xb = inputs.bf16_bits(x)
+    compare.check_mixes(np64(m), oracle.hc_mixes(xb, w.cpu().numpy()))
+    o_pre, o_post, o_comb = oracle.hc_split_sinkhorn(np64(m), sc.cpu().numpy(),
+                                                     base.cpu().numpy(), 8, 20, 1e-6)
+    compare.check_abs(np64(pre), o_pre, 1e-5, "pre")
+    compare.check_abs(np64(post), o_post, 1e-5, "post")
+    compare.check_abs(np64(comb), o_comb, 1e-5, "comb")
+    want, _, mag = oracle.hc_pre(xb, np64(pre))
+    compare.check_bf16(inputs.bf16_bits(y), want, mag, 8, "y")

@@ -63,16 +63,26 @@ def noalloc(L, x, w, sc, base, iters=20, eps=1e-6, norm_eps=1e-20):
 
 @pytest.mark.parametrize("n,hc,d", [(37, 4, 64), (300, 8, 5120)])
 def test_noalloc_equals_hc_mixes_pre_on_the_general_path(L, n, hc, d):
-    # these shapes take the general three-kernel path in hc_mixes_pre too:
-    # same kernels, same inputs, so the results are identical
+    # the no-allocation entry runs the general three-kernel path with the
+    # CUDA-core projection; hc_mixes_pre runs the same kernels when the path
+    # is pinned to it: same inputs, so the results are identical
+    import os
     import sinkhorn_mixing_gb300 as m
-    for call, seed in enumerate((1, 2)):
-        x, w, sc, base = case(n, hc, d, seed + 10 * hc)
-        got = noalloc(L, x, w, sc, base)
-        want = m.hc_mixes_pre(x, w, sc, base)[:4]
-        torch.cuda.synchronize()
-        for a, b in zip(got, want):
-            assert torch.equal(a, b), "call %d differs" % call
+    old = os.environ.get("HCMIX_PATH")
+    os.environ["HCMIX_PATH"] = "ffma"
+    try:
+        for call, seed in enumerate((1, 2)):
+            x, w, sc, base = case(n, hc, d, seed + 10 * hc)
+            got = noalloc(L, x, w, sc, base)
+            want = m.hc_mixes_pre(x, w, sc, base)[:4]
+            torch.cuda.synchronize()
+            for a, b in zip(got, want):
+                assert torch.equal(a, b), "call %d differs" % call
+    finally:
+        if old is None:
+            os.environ.pop("HCMIX_PATH", None)
+        else:
+            os.environ["HCMIX_PATH"] = old
 
 
 def test_noalloc_matches_fused_entry_point_within_tolerance(L):
