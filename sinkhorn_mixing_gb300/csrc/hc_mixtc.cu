@@ -58,7 +58,7 @@ template <int HC>
 struct Cfg {
     static constexpr int kMix = (2 + HC) * HC;      // 24 or 80
     static constexpr int kNW = 2 * kMix;            // B rows: hi then lo
-    static constexpr int kStages = HC == 8 ? 3 : 6;
+    static constexpr int kStages = HC == 8 ? 4 : 6;
     static constexpr int kWfBytes = kMix * kK * 4;  // fp32 W sub-tile
     static constexpr int kWbBytes = kNW * kK * 2;   // bf16 hi/lo sub-tile
     static constexpr int kTmemCols = HC == 8 ? 512 : 128;  // >= 2 * kNW, power of 2
