@@ -255,6 +255,60 @@ __global__ void __launch_bounds__(256) k_post(int64_t n, Units un, const uint4 *
     }
 }
 
+// ------------------------------------------------------ k_post_shared
+// k_post for large hc (8): the token's post and comb live in a per-warp slot
+// of shared memory and are read as broadcasts, instead of 72 registers per
+// lane, so that two CTAs fit on an SM (with them in registers the kernel
+// needed 187 registers and ran one CTA per SM).  Same arithmetic and order
+// as k_post.
+template <int HC>
+__global__ void __launch_bounds__(256, 2) k_post_shared(int64_t n, Units un,
+                                                         const uint4 *__restrict__ out,
+                                                         const uint4 *res,
+                                                         const float *__restrict__ post,
+                                                         const float *__restrict__ comb, uint4 *y) {
+    __shared__ float coef[8][HC * HC + HC];  // per warp: comb [j][k], then post [k]
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t units = n * un.nseg;
+    float *cf = coef[wib];
+    for (int64_t u = warp; u < units; u += nwarps) {
+        const int64_t t = u / un.nseg, s = u % un.nseg;
+        const int64_t v0 = s * un.seg, v1 = min(un.nv, v0 + un.seg);
+        __syncwarp();
+        for (int q = lane; q < HC * HC; q += 32) cf[q] = __ldg(comb + t * HC * HC + q);
+        if (lane < HC) cf[HC * HC + lane] = __ldg(post + t * HC + lane);
+        __syncwarp();
+        const uint4 *ot = out + t * un.nv;
+        const uint4 *rt = res + t * HC * un.nv;
+        uint4 *yt = y + t * HC * un.nv;
+        for (int64_t v = v0 + lane; v < v1; v += 32) {
+            uint4 o = ld_stream(ot + v), r[HC];
+#pragma unroll
+            for (int j = 0; j < HC; ++j) r[j] = ld_stream(rt + j * un.nv + v);
+            float of[8], rf[HC][8];
+            unpack8(o, of);
+#pragma unroll
+            for (int j = 0; j < HC; ++j) unpack8(r[j], rf[j]);
+#pragma unroll
+            for (int k = 0; k < HC; ++k) {
+                const float pk = cf[HC * HC + k];
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = pk * of[e];
+#pragma unroll
+                for (int j = 0; j < HC; ++j) {
+                    const float c = cf[j * HC + k];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(c, rf[j][e], acc[e]);
+                }
+                st_stream(yt + k * un.nv + v, pack8(acc));
+            }
+        }
+    }
+}
+
 // Split each token's nv vectors into segments so that there are enough
 // warp units to fill the GPU when n is small.
 Units make_units(int64_t n, int64_t nv, int sms) {
@@ -328,7 +382,7 @@ cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
     if (hc == 4)
         k_post<4, 2><<<grid, 256, 0, s>>>(n, un, ov, rv, post, comb, yv);
     else
-        k_post<8, 1><<<grid, 256, 0, s>>>(n, un, ov, rv, post, comb, yv);
+        k_post_shared<8><<<grid, 256, 0, s>>>(n, un, ov, rv, post, comb, yv);
     return launched();
 }
 
