@@ -152,6 +152,17 @@ size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
  */
 hc_status hc_device_error(unsigned int *flags, int clear);
 
+/*
+ * hc_selftest_wait_timeout -- diagnostic with no counterpart on the pages:
+ * enqueues one CTA that waits, through the same bounded wait the kernels
+ * use, on a barrier nothing arrives on, so the wait gives up after
+ * limit_ns nanoseconds and sets bit 0 of the error word (read it with
+ * hc_device_error).  It shows that a wait that cannot finish ends with a
+ * status instead of a hang or a fault, and that the context stays usable.
+ * 1 <= limit_ns <= 1e9 (else HC_ERR_INVALID_ARG).
+ */
+hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream);
+
 /* Device floats that libhcmix.so keeps for hc_mixes_pre_noalloc: a fixed
  * array of 4 MiB on every GPU that loads the library, held until exit. */
 #define HC_NOALLOC_SCRATCH_FLOATS (1u << 20)

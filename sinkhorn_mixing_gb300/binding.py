@@ -54,6 +54,8 @@ def lib():
         L.hc_workspace_bytes.restype = ctypes.c_size_t
         L.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         L.hc_launch_count.restype = ctypes.c_uint64
+        L.hc_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.hc_selftest_wait_timeout.restype = i32
         for f in ("hc_mixes", "hc_split_sinkhorn", "hc_pre", "hc_post", "hc_mixes_pre",
                   "hc_device_error"):
             getattr(L, f).restype = i32
@@ -265,3 +267,12 @@ def hc_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint(0)
     _check(lib().hc_device_error(ctypes.byref(v), 1 if clear else 0), "hc_device_error")
     return int(v.value)
+
+
+def hc_selftest_wait_timeout(limit_ns: int = 1000000, device=None, stream=None) -> None:
+    """Enqueues the library's bounded-wait self-test: a wait that can only
+    time out, after which hc_device_error() reports bit 0."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    with _on_device(dev):
+        _check(lib().hc_selftest_wait_timeout(int(limit_ns), _stream(dev, stream)),
+               "hc_selftest_wait_timeout")

@@ -301,6 +301,14 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float
     return from_cuda(e);
 }
 
+hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream) {
+    if (limit_ns < 1 || limit_ns > 1000000000ull) return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    return from_cuda(
+        hc::launch_wait_timeout(limit_ns, di, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 hc_status hc_device_error(unsigned int *flags, int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return HC_ERR_CUDA;
     unsigned int v = 0;

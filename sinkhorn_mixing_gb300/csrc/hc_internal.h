@@ -65,4 +65,7 @@ cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
                         const uint16_t *res, const float *post, const float *comb, uint16_t *y,
                         const DeviceInfo &di, cudaStream_t s);
 
+// Diagnostic (hc_selftest.cu): one CTA whose bounded wait can only time out.
+cudaError_t launch_wait_timeout(uint64_t limit_ns, const DeviceInfo &di, cudaStream_t s);
+
 }  // namespace hc

@@ -71,16 +71,17 @@ __device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) 
 }
 
 // Bounded wait for the phase of `bar` with the given parity.  Returns false
-// (and raises the abort flag) on timeout or when the CTA is already aborting.
+// (and raises the abort flag) on timeout or when the CTA is already aborting;
+// a timeout also sets bit 0 of the device error word `err`.
 template <bool kClusterScope>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort,
-                                         unsigned int *err) {
+                                         unsigned int *err, uint64_t limit_ns = kTimeoutNs) {
     if (kClusterScope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
     const uint64_t t0 = gtimer();
     while (true) {
         if (kClusterScope ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
         if (*abort) return false;
-        if (gtimer() - t0 > kTimeoutNs) {
+        if (gtimer() - t0 > limit_ns) {
             *abort = 1;
             atomicOr(err, kErrWaitTimeout);
             return false;

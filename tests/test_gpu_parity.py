@@ -272,13 +272,21 @@ def test_full_chain_tiny_end_to_end(hc):
         np.testing.assert_allclose(g, want, rtol=2 ** -7, atol=1e-3)
 
 
-def test_guard_bytes_untouched(hc):
-    n, d = 37, 136
+@pytest.mark.parametrize("n,H,d,path", [
+    (37, 4, 136, "general (CUDA-core projection)"),
+    (37, 4, 5120, "decode kernel"),
+    (200, 4, 2048, "fused kernel"),
+    (200, 4, 2304, "tensor-core projection, hc=4"),
+    (150, 8, 1024, "tensor-core projection and shared-coefficient post, hc=8"),
+])
+def test_guard_bytes_untouched(hc, n, H, d, path):
+    # no kernel writes outside its outputs: 64 sentinel elements on each side
+    mix = (2 + H) * H
     g = torch.Generator(device="cuda").manual_seed(11)
-    x = torch.randn((n, 4, d), device="cuda", generator=g).to(torch.bfloat16)
-    w = torch.randn((24, 4 * d), device="cuda", generator=g) / (4 * d) ** 0.5
+    x = torch.randn((n, H, d), device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn((mix, H * d), device="cuda", generator=g) / (H * d) ** 0.5
     scale = torch.ones(3, device="cuda")
-    base = torch.zeros(24, device="cuda")
+    base = torch.zeros(mix, device="cuda")
     pad = 64
 
     def padded(shape, dtype):
@@ -286,15 +294,15 @@ def test_guard_bytes_untouched(hc):
         buf = torch.full((numel + 2 * pad,), 77, dtype=dtype, device="cuda")
         return buf, buf[pad:pad + numel].view(shape)
 
-    bufs = [padded((n, 24), torch.float32), padded((n, 4), torch.float32),
-            padded((n, 4), torch.float32), padded((n, 4, 4), torch.float32),
-            padded((n, d), torch.bfloat16), padded((n, 4, d), torch.bfloat16)]
+    bufs = [padded((n, mix), torch.float32), padded((n, H), torch.float32),
+            padded((n, H), torch.float32), padded((n, H, H), torch.float32),
+            padded((n, d), torch.bfloat16), padded((n, H, d), torch.bfloat16)]
     (bm, m), (bp, pre), (bq, post), (bc, comb), (by, y), (bz, z) = bufs
     hc.hc_mixes_pre(x, w, scale, base, mixes=m, pre=pre, post=post, comb=comb, y=y)
     hc.hc_post(y, x, post, comb, y=z)
     torch.cuda.synchronize()
     for buf, _ in bufs:
-        assert torch.all(buf[:pad] == 77) and torch.all(buf[-pad:] == 77)
+        assert torch.all(buf[:pad] == 77) and torch.all(buf[-pad:] == 77), path
 
 
 def test_runs_on_a_side_stream(hc):
@@ -321,3 +329,18 @@ def test_errors_raise_and_launch_nothing(hc):
         hc.hc_split_sinkhorn(torch.zeros((4, 24), device="cuda"), torch.ones(3, device="cuda"),
                              torch.zeros(24, device="cuda"), 4, 0)   # iters < 1
     assert hc.hc_launch_count() == before
+
+
+def test_bounded_wait_reports_a_timeout_and_the_context_survives(hc):
+    # a wait that nothing can complete runs out after 2 ms and sets bit 0 of
+    # the device error word instead of hanging; later calls work normally
+    hc.hc_device_error(clear=True)
+    hc.hc_selftest_wait_timeout(2_000_000)
+    assert hc.hc_device_error(clear=True) & 1 == 1
+    wl = WL["tiny"]
+    s = streams(wl)
+    p = params(wl)
+    y = hc.hc_mixes_pre(s["x"], p["w"], p["hc_scale"], p["hc_base"])[0]
+    torch.cuda.synchronize()
+    assert hc.hc_device_error(clear=True) == 0
+    assert bool(torch.isfinite(y.float()).all())
