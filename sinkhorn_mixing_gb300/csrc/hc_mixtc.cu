@@ -3,26 +3,29 @@
 // ("Mix projection" page: the formula for m, Block.hc_mixes).
 //
 // Work decomposition
-//   * Persistent CTAs, one per SM, take 128-token tiles in turn.  A tile's
-//     feature axis is walked in stages of 64 features: TMA brings the x
-//     sub-tile [128 tokens x 64] (128-byte swizzled, K-major) and the W
-//     sub-tile [mix x 64] (fp32 rows) into a ring of kStages slots.
+//   * Persistent CTAs, one per SM, take units of kTPU consecutive 128-token
+//     tiles in turn.  A unit's feature axis is walked in stages of 64
+//     features: TMA brings each tile's x sub-tile [128 tokens x 64]
+//     (128-byte swizzled, K-major) and one W sub-tile [mix x 64] (fp32 rows)
+//     into a ring of kStages slots.  An SM's intake of W is what bounds the
+//     kernel at hc = 8 (W is 13 MB, read from L2 once per unit), so there a
+//     unit is two tiles sharing every W stage.
 //   * 4 convert warps split the W sub-tile into bf16 hi rows (bf16(W)) and lo
 //     rows (bf16(W - hi)) in the swizzled K-major layout the tensor core
 //     reads, so no converted copy of W is kept in memory.
-//   * Per stage, 4 tcgen05.mma (M = 128 tokens, N = 2*mix rows of hi and lo,
-//     K = 16) accumulate x.(W_hi + W_lo) in TMEM (binary32).  bf16 x is exact
+//   * Per stage and tile, 4 tcgen05.mma (M = 128 tokens, N = 2*mix rows of hi
+//     and lo, K = 16) accumulate x.(W_hi + W_lo) in TMEM (binary32).  bf16 x is exact
 //     and hi + lo carries ~16 mantissa bits of W.  The tensor core's own
 //     accumulation loses about one binary32 unit per step in one direction, so
-//     a tile's feature axis is cut into parts of kPart stages (256 MMA steps):
-//     each part accumulates in one of two TMEM buffers and the epilogue adds
-//     the parts in binary32 registers (round to nearest) while the MMAs go on
-//     in the other buffer.  One chain over 40,960 features was off by 1.4e-4
-//     relative.
+//     a unit's feature axis is cut into parts of kPart stages (256 MMA steps):
+//     each part accumulates in TMEM and the epilogue adds the parts in
+//     binary32 registers (round to nearest); with one tile per unit two TMEM
+//     buffers let the MMAs go on during the read-out.  One chain over 40,960
+//     features was off by 1.4e-4 relative.
 //   * 4 square warps add x^2 per token from the same sub-tiles.
-//   * 4 epilogue warps (one per TMEM lane quadrant, 32 tokens each) read the
-//     accumulators, add hi and lo, scale by r = 1/sqrt(mean x^2 + eps) and
-//     write the mix numbers.
+//   * 4 epilogue warps per tile (one per TMEM lane quadrant, 32 tokens each)
+//     read the accumulators, add hi and lo, scale by r = 1/sqrt(mean x^2 +
+//     eps) and write the mix numbers.
 // Every wait is bounded; a timeout sets the CTA's abort flag and bit 0 of the
 // device error word, and all roles run to the teardown (no trap; TMEM and
 // in-flight copies are always waited for).
@@ -43,89 +46,102 @@ constexpr int kTok = 128;                // tokens per tile (MMA M)
 constexpr int kK = 64;                   // features per stage
 constexpr int kXBytes = kTok * kK * 2;   // x sub-tile, 16 KB
 constexpr int kPart = 64;                // stages per tensor-core accumulation chain
-constexpr int kThreads = 14 * 32;
-// warp roles
+// warp roles: 0 producer, 1 MMA, 2..5 squares (32 tokens of every tile each),
+// 6, 7 and the two after the epilogue warps convert W, 8.. epilogue (4 per
+// tile of a unit, one per TMEM lane quadrant)
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
-constexpr int kWarpSq0 = 2;              // 2..5: sums of squares, 32 tokens each
-constexpr int kWarpEpi0 = 8;             // 8..11: TMEM lane quadrants 0..3
-__host__ __device__ constexpr bool is_convert_warp(int w) {
-    return w == 6 || w == 7 || w == 12 || w == 13;
-}
-__host__ __device__ constexpr int convert_index(int w) { return w < 8 ? w - 6 : w - 10; }
+constexpr int kWarpSq0 = 2;
+constexpr int kWarpEpi0 = 8;
 
 template <int HC>
 struct Cfg {
     static constexpr int kMix = (2 + HC) * HC;      // 24 or 80
     static constexpr int kNW = 2 * kMix;            // B rows: hi then lo
-    static constexpr int kStages = HC == 8 ? 4 : 6;
+    static constexpr int kTPU = HC == 8 ? 2 : 1;    // tiles per unit
+    static constexpr int kAccBufs = kTPU == 1 ? 2 : 1;
+    static constexpr int kStages = HC == 8 ? 3 : 6;
     static constexpr int kWfBytes = kMix * kK * 4;  // fp32 W sub-tile
     static constexpr int kWbBytes = kNW * kK * 2;   // bf16 hi/lo sub-tile
-    static constexpr int kTmemCols = HC == 8 ? 512 : 128;  // >= 2 * kNW, power of 2
+    static constexpr int kXStage = kTPU * kXBytes;  // x sub-tiles of a stage
+    static constexpr int kTmemCols = HC == 8 ? 512 : 128;
+    static constexpr int kWarps = 10 + 4 * kTPU;
+    static constexpr int kThreads = kWarps * 32;
     // tcgen05 instruction descriptor: D f32, A/B bf16, K-major, N = kNW, M = 128
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                        ((uint32_t)(kNW >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     static_assert(kNW % 16 == 0 && kNW <= 256, "MMA N");
-    static_assert(2 * kNW <= kTmemCols, "two accumulator buffers");
+    static_assert(kAccBufs * kTPU * kNW <= kTmemCols, "accumulators fit in TMEM");
     static_assert(kWbBytes % 1024 == 0 && kWfBytes % 1024 == 0, "swizzle atoms and TMA alignment");
+    __host__ __device__ static constexpr bool is_convert(int w) {
+        return w == 6 || w == 7 || w == kWarpEpi0 + 4 * kTPU || w == kWarpEpi0 + 4 * kTPU + 1;
+    }
+    __host__ __device__ static constexpr int convert_index(int w) {
+        return w < kWarpEpi0 ? w - 6 : w - (kWarpEpi0 + 4 * kTPU) + 2;
+    }
 };
 
 struct MixParams {
     int64_t n;
     int F;
-    int nk;         // stages per tile, F / 64
+    int nk;         // stages per unit, F / 64
     int num_tiles;
+    int num_units;
     float norm_eps;
-    float* mixes;
+    float *mixes;
     unsigned int *err;
 };
 
 template <int HC>
 __host__ __device__ constexpr size_t ring_bytes() {
-    return (size_t)Cfg<HC>::kStages * (kXBytes + Cfg<HC>::kWbBytes + Cfg<HC>::kWfBytes);
+    return (size_t)Cfg<HC>::kStages * (Cfg<HC>::kXStage + Cfg<HC>::kWbBytes + Cfg<HC>::kWfBytes);
 }
 
 // barrier indices
 template <int HC>
 struct Bars {
     static constexpr int S = Cfg<HC>::kStages;
+    static constexpr int A = Cfg<HC>::kAccBufs;
     static constexpr int full(int s) { return s; }
     static constexpr int conv(int s) { return S + s; }
     static constexpr int empty(int s) { return 2 * S + s; }
     static constexpr int acc_full(int b) { return 3 * S + b; }
-    static constexpr int acc_empty(int b) { return 3 * S + 2 + b; }
-    static constexpr int sq_full(int b) { return 3 * S + 4 + b; }
-    static constexpr int sq_empty(int b) { return 3 * S + 6 + b; }
-    static constexpr int drain = 3 * S + 8;
+    static constexpr int acc_empty(int b) { return 3 * S + A + b; }
+    static constexpr int sq_full(int b) { return 3 * S + 2 * A + b; }
+    static constexpr int sq_empty(int b) { return 3 * S + 2 * A + 2 + b; }
+    static constexpr int drain = 3 * S + 2 * A + 4;
     static constexpr int count = drain + 1;
 };
 
 template <int HC>
 __host__ __device__ constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + ring_bytes<HC>() + 2 * kTok * 4 + Bars<HC>::count * 8 + 16;
+    return 1024 /* alignment slack */ + ring_bytes<HC>() + 2 * Cfg<HC>::kTPU * kTok * 4 +
+           Bars<HC>::count * 8 + 16;
 }
 
 template <int HC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
     k_mixtc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
             const MixParams p) {
     using C = Cfg<HC>;
     using B = Bars<HC>;
     constexpr int S = C::kStages;
+    constexpr int TPU = C::kTPU;
+    constexpr int AB = C::kAccBufs;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint8_t *xr = base;                               // [S][128 x 64] bf16, swizzled
-    uint8_t *wb = xr + (size_t)S * kXBytes;           // [S][kNW x 64] bf16, swizzled
+    uint8_t *xr = base;                               // [S][TPU][128 x 64] bf16, swizzled
+    uint8_t *wb = xr + (size_t)S * C::kXStage;        // [S][kNW x 64] bf16, swizzled
     float *wf = reinterpret_cast<float *>(wb + (size_t)S * C::kWbBytes);  // [S][kMix][64]
-    float *sq = wf + (size_t)S * C::kMix * kK;        // [2][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sq + 2 * kTok);
+    float *sq = wf + (size_t)S * C::kMix * kK;        // [2][TPU][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sq + 2 * TPU * kTok);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B::count);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *abort = abort_word;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = (int)blockIdx.x < p.num_tiles
-                      ? (p.num_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
+    const int U = (int)blockIdx.x < p.num_units
+                      ? (p.num_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x
                       : 0;
     auto bar = [&](int i) { return su32(bars + i); };
 
@@ -136,11 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(B::conv(s)), 4);
             mbar_init(bar(B::empty(s)), 5);  // MMA commit + 4 square warps
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < AB; ++b) {
             mbar_init(bar(B::acc_full(b)), 1);
-            mbar_init(bar(B::acc_empty(b)), 4);
+            mbar_init(bar(B::acc_empty(b)), 4 * TPU);
+        }
+        for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B::sq_full(b)), 4);
-            mbar_init(bar(B::sq_empty(b)), 4);
+            mbar_init(bar(B::sq_empty(b)), 4 * TPU);
         }
         mbar_init(bar(B::drain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -163,8 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s) last_use[s] = -1;
             bool ok = true;
             uint32_t q = 0;
-            for (int it = 0; it < T && ok; ++it) {
-                const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+            for (int it = 0; it < U && ok; ++it) {
+                const int unit = (int)blockIdx.x + it * (int)gridDim.x;
                 for (int kc = 0; kc < p.nk; ++kc, ++q) {
                     const int slot = (int)(q % S);
                     const uint32_t use = q / S;
@@ -172,9 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(B::full(slot)), (uint32_t)(kXBytes + C::kWfBytes));
-                    tma_load_2d(su32(xr + (size_t)slot * kXBytes), &tm_x, kc * kK, tile * kTok,
-                                bar(B::full(slot)));
+                    mbar_expect_tx(bar(B::full(slot)), (uint32_t)(C::kXStage + C::kWfBytes));
+                    // a unit's second tile past the last token reads zeros
+#pragma unroll
+                    for (int v = 0; v < TPU; ++v)
+                        tma_load_2d(su32(xr + (size_t)slot * C::kXStage + v * kXBytes), &tm_x,
+                                    kc * kK, (unit * TPU + v) * kTok, bar(B::full(slot)));
                     tma_load_2d(su32(wf + (size_t)slot * C::kMix * kK), &tm_w, kc * kK, 0,
                                 bar(B::full(slot)));
                     last_use[slot] = (int)use;
@@ -189,13 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             bool ok = true;
             uint32_t q = 0, gp = 0;  // stage and accumulation-part counters
-            for (int it = 0; it < T && ok; ++it) {
+            for (int it = 0; it < U && ok; ++it) {
                 for (int k0 = 0; k0 < p.nk && ok; k0 += kPart, ++gp) {
-                    const int b = (int)(gp & 1);
-                    if (!wait_bar<false>(bar(B::acc_empty(b)), ((gp >> 1) & 1) ^ 1, abort, p.err))
+                    const int b = (int)(gp % AB);
+                    if (!wait_bar<false>(bar(B::acc_empty(b)), ((gp / AB) & 1) ^ 1, abort, p.err))
                         break;
                     tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(b * C::kNW);
                     const int k1 = k0 + kPart < p.nk ? k0 + kPart : p.nk;
                     for (int kc = k0; kc < k1; ++kc, ++q) {
                         const int slot = (int)(q % S);
@@ -206,12 +226,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a0 = su32(xr + (size_t)slot * kXBytes);
                         const uint32_t b0 = su32(wb + (size_t)slot * C::kWbBytes);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
-                                     C::kIdesc, ((kc - k0) | k) != 0);
+                        for (int v = 0; v < TPU; ++v) {
+                            const uint32_t a0 = su32(xr + (size_t)slot * C::kXStage + v * kXBytes);
+                            const uint32_t d_tmem = tmem + (uint32_t)((b * TPU + v) * C::kNW);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                mma_bf16(d_tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k),
+                                         C::kIdesc, ((kc - k0) | k) != 0);
+                        }
                         mma_commit(bar(B::empty(slot)));
                     }
                     if (!ok) break;
@@ -222,13 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(B::drain));
             wait_bar<false>(bar(B::drain), 0, abort, p.err);
         }
-    } else if (is_convert_warp(warp)) {
+    } else if (C::is_convert(warp)) {
         // W sub-tile (fp32 rows of 64) -> bf16 hi rows 0..kMix-1 and lo rows
         // kMix..2kMix-1, 8 features per 16-byte chunk, swizzled K-major.
-        const int ci = convert_index(warp) * 32 + lane;
+        const int ci = C::convert_index(warp) * 32 + lane;
         uint32_t q = 0;
         bool ok = true;
-        for (int it = 0; it < T && ok; ++it) {
+        for (int it = 0; it < U && ok; ++it) {
             for (int kc = 0; kc < p.nk; ++kc, ++q) {
                 const int slot = (int)(q % S);
                 if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::full(slot)), (q / S) & 1,
@@ -267,15 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
-        // Sums of squares: warp 2+g takes tokens 32g..32g+31, lane = token,
-        // chunks in swizzle order so 8 consecutive lanes hit 8 bank groups.
+        // Sums of squares: warp 2+g takes tokens 32g..32g+31 of every tile of
+        // the unit, lane = token, chunks in swizzle order so 8 consecutive
+        // lanes hit 8 bank groups.
         const int i = 32 * (warp - kWarpSq0) + lane;
         uint32_t q = 0;
         bool ok = true;
-        for (int it = 0; it < T && ok; ++it) {
-            const int b = it & 1;
+        for (int it = 0; it < U && ok; ++it) {
+            const int bs = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            float ss = 0.f;
+            float ss[TPU];
+#pragma unroll
+            for (int v = 0; v < TPU; ++v) ss[v] = 0.f;
             for (int kc = 0; kc < p.nk; ++kc, ++q) {
                 const int slot = (int)(q % S);
                 if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::full(slot)), (q / S) & 1,
@@ -283,46 +310,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t row = su32(xr + (size_t)slot * kXBytes) + (i >> 3) * 1024 + (i & 7) * 128;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    float f[8];
-                    unpack8(lds128(row + ((m ^ (i & 7)) << 4)), f);
+                for (int v = 0; v < TPU; ++v) {
+                    const uint32_t row = su32(xr + (size_t)slot * C::kXStage + v * kXBytes) +
+                                         (i >> 3) * 1024 + (i & 7) * 128;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                    for (int m = 0; m < 8; ++m) {
+                        float f[8];
+                        unpack8(lds128(row + ((m ^ (i & 7)) << 4)), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss[v] = fmaf(f[e], f[e], ss[v]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B::empty(slot)));
             }
             if (!ok) break;
             if (!__all_sync(0xFFFFFFFFu,
-                            wait_bar<false>(bar(B::sq_empty(b)), (use & 1) ^ 1, abort, p.err)))
+                            wait_bar<false>(bar(B::sq_empty(bs)), (use & 1) ^ 1, abort, p.err)))
                 break;
-            sq[b * kTok + i] = ss;
+#pragma unroll
+            for (int v = 0; v < TPU; ++v) sq[(bs * TPU + v) * kTok + i] = ss[v];
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B::sq_full(b)));
+            if (lane == 0) mbar_arrive(bar(B::sq_full(bs)));
         }
-    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
-        // TMEM lanes 32*(warp % 4).. = tokens of the tile; the parts of a
-        // tile are added in registers, then scaled by r and written.
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4 * TPU) {
+        // Tile v of the unit, TMEM lanes 32*(warp % 4).. = its tokens; the
+        // parts of the unit are added in registers, then scaled by r and
+        // written.
+        const int v = (warp - kWarpEpi0) >> 2;
         const int i = 32 * (warp & 3) + lane;
         const uint32_t tlane = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t gp = 0;
         bool ok = true;
-        for (int it = 0; it < T && ok; ++it) {
-            const int tile = (int)blockIdx.x + it * (int)gridDim.x;
+        for (int it = 0; it < U && ok; ++it) {
+            const int unit = (int)blockIdx.x + it * (int)gridDim.x;
             float m[C::kMix];
 #pragma unroll
             for (int k = 0; k < C::kMix; ++k) m[k] = 0.f;
             for (int k0 = 0; k0 < p.nk; k0 += kPart, ++gp) {
-                const int b = (int)(gp & 1);
-                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::acc_full(b)), (gp >> 1) & 1,
+                const int b = (int)(gp % AB);
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::acc_full(b)), (gp / AB) & 1,
                                                              abort, p.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + tlane + (uint32_t)(b * C::kNW);
+                const uint32_t taddr = tmem + tlane + (uint32_t)((b * TPU + v) * C::kNW);
 #pragma unroll
                 for (int g = 0; g < C::kMix / 8; ++g) {
                     float hi[8], lo[8];
@@ -341,16 +375,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int bs = it & 1;
             if (!__all_sync(0xFFFFFFFFu, wait_bar<false>(bar(B::sq_full(bs)), use & 1, abort, p.err)))
                 break;
-            const float r = rsqrtf(sq[bs * kTok + i] / (float)p.F + p.norm_eps);
+            const float r = rsqrtf(sq[(bs * TPU + v) * kTok + i] / (float)p.F + p.norm_eps);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B::sq_empty(bs)));
-            const int64_t t = (int64_t)tile * kTok + i;
+            const int64_t t = ((int64_t)unit * TPU + v) * kTok + i;
             if (t < p.n) {
                 float4 *dst = reinterpret_cast<float4 *>(p.mixes + t * C::kMix);
 #pragma unroll
-                for (int v = 0; v < C::kMix / 4; ++v)
-                    dst[v] = make_float4(m[4 * v] * r, m[4 * v + 1] * r, m[4 * v + 2] * r,
-                                         m[4 * v + 3] * r);
+                for (int q4 = 0; q4 < C::kMix / 4; ++q4)
+                    dst[q4] = make_float4(m[4 * q4] * r, m[4 * q4 + 1] * r, m[4 * q4 + 2] * r,
+                                          m[4 * q4 + 3] * r);
             }
         }
     }
@@ -436,11 +470,12 @@ cudaError_t launch(int64_t n, int64_t d, float norm_eps, const uint16_t *x, cons
     p.F = (int)F;
     p.nk = (int)(F / kK);
     p.num_tiles = (int)((n + kTok - 1) / kTok);
+    p.num_units = (p.num_tiles + Cfg<HC>::kTPU - 1) / Cfg<HC>::kTPU;
     p.norm_eps = norm_eps;
     p.mixes = mixes;
     p.err = di.err_word;
-    const int grid = p.num_tiles < di.sms ? p.num_tiles : di.sms;
-    k_mixtc<HC><<<grid, kThreads, smem_bytes<HC>(), s>>>(tm_x, tm_w, p);
+    const int grid = p.num_units < di.sms ? p.num_units : di.sms;
+    k_mixtc<HC><<<grid, Cfg<HC>::kThreads, smem_bytes<HC>(), s>>>(tm_x, tm_w, p);
     return launched();
 }
 
