@@ -40,10 +40,11 @@ def _load():
         lib.orc_hc_split_sinkhorn.argtypes = [i64, i32, i32, f64, P, P, P, P, P, P]
         lib.orc_hc_pre.argtypes = [i64, i32, i64, P, P, P, P, P]
         lib.orc_hc_post.argtypes = [i64, i32, i64, P, P, P, P, P, P, P]
+        lib.orc_hc_rmsnorm.argtypes = [i64, i64, P, P, f64, P, P]
         lib.orc_num_threads.restype = i32
         lib.orc_set_num_threads.argtypes = [i32]
         for f in ("orc_hc_mixes", "orc_hc_split_sinkhorn", "orc_hc_pre",
-                  "orc_hc_post", "orc_set_num_threads"):
+                  "orc_hc_post", "orc_hc_rmsnorm", "orc_set_num_threads"):
             getattr(lib, f).restype = None
         _lib = lib
     return _lib
@@ -123,6 +124,20 @@ def hc_pre(x_bits, pre):
     mag = np.empty((n, d))
     _load().orc_hc_pre(n, hc, d, _ptr(x), _ptr(p), _ptr(y), _ptr(yb), _ptr(mag))
     return y, yb, mag
+
+
+def hc_rmsnorm(y_bits, weight, eps=1e-20):
+    """RMSNorm of the bf16 collapse output (standard form; not on the pages):
+    y_bits uint16 [n, d], weight float32 [d] -> (out float64 [n, d], out bf16
+    bits [n, d])."""
+    y = _c(y_bits, np.uint16)
+    n, d = y.shape
+    g = _c(weight, np.float32)
+    assert g.shape == (d,)
+    out = np.empty((n, d))
+    ob = np.empty((n, d), dtype=np.uint16)
+    _load().orc_hc_rmsnorm(n, d, _ptr(y), _ptr(g), float(eps), _ptr(out), _ptr(ob))
+    return out, ob
 
 
 def hc_post(out_bits, res_bits, post, comb):

@@ -17,6 +17,9 @@
  *     a column normalisation and iters-1 rounds of row-then-column
  *     normalisation, every later denominator being (sum + eps).
  *   - "Mix projection" page, Block.hc_pre and Block.hc_post (model.py 948-966).
+ *   - The RMSNorm the block applies to hc_pre's output (attn_norm / ffn_norm)
+ *     is named but not shown on the pages: the standard form is taken (see
+ *     orc_hc_rmsnorm).
  *
  * Arithmetic: every step in double.  bf16 inputs are decoded exactly; bf16
  * outputs are rounded once, directly from the double value, to nearest-even.
@@ -245,6 +248,34 @@ void orc_hc_pre(int64_t n, int hc, int64_t d, const uint16_t *x,
  * out: [n, d] bf16 bits; res: [n, hc, d] bf16 bits; post: [n, hc] double;
  * comb: [n, hc, hc] double; y: [n, hc, d] double (may be NULL);
  * y_bf16: [n, hc, d] bits (may be NULL); mag: [n, hc, d] (may be NULL). */
+/*
+ * RMSNorm of the collapsed sublayer input (the block's attn_norm / ffn_norm
+ * applied to hc_pre's output).  Its body is not on the pages; the plain
+ * standard form is taken: with y the bf16 collapse output decoded exactly,
+ *   out_c = y_c * g_c / sqrt(mean_c(y_c^2) + eps),
+ * rounded once to bf16 (nearest-even).  out (double) and out_bf16 may be NULL.
+ */
+void orc_hc_rmsnorm(int64_t n, int64_t d, const uint16_t *y, const float *g, double eps,
+                    double *out, uint16_t *out_bf16)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        double ss = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            const double v = orc_bf16_to_double(y[t * d + c]);
+            ss += v * v;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)d + eps);
+        for (int64_t c = 0; c < d; ++c) {
+            const double v = orc_bf16_to_double(y[t * d + c]) * (double)g[c] * inv;
+            if (out)
+                out[t * d + c] = v;
+            if (out_bf16)
+                out_bf16[t * d + c] = orc_double_to_bf16(v);
+        }
+    }
+}
+
 void orc_hc_post(int64_t n, int hc, int64_t d, const uint16_t *out,
                  const uint16_t *res, const double *post, const double *comb,
                  double *y, uint16_t *y_bf16, double *mag)

@@ -501,3 +501,66 @@ def test_printed_constants_and_parameter_counts():
     assert wl.mix_hc == k["mix_hc"] and wl.F == k["flat_features"]
     assert inputs.make_params(wl)["w"].numel() == k["w_mix_params"]
     assert wl.hc + 1 == k["pre_params_per_instance"]  # hc offsets + one scale
+
+
+# ---------------------------------------------------- RMSNorm of the collapse
+# The block normalises hc_pre's output before the sublayer (attn_norm /
+# ffn_norm); the pages name it but do not show it, so the oracle takes the
+# standard form out = y * g / sqrt(mean(y^2) + eps).  These pins would catch a
+# sum in place of the mean, a missing square root, a dropped weight or eps,
+# or a normalisation over the wrong axis.
+
+def test_rmsnorm_constant_row_with_unit_weight_is_its_sign():
+    y = bf16_of(np.array([[3.0] * 16, [-0.25] * 16]))
+    out, bits = oracle.hc_rmsnorm(y, np.ones(16, np.float32))
+    assert np.all(bits[0] == bf16_of([1.0])[0]) and np.all(bits[1] == bf16_of([-1.0])[0])
+    np.testing.assert_allclose(out, [[1.0] * 16, [-1.0] * 16], rtol=1e-15)
+
+
+def test_rmsnorm_unit_weight_output_has_unit_mean_square():
+    y = bf16_of(rng(61).normal(0, 3, (5, 384)))
+    out, _ = oracle.hc_rmsnorm(y, np.ones(384, np.float32))
+    np.testing.assert_allclose((out ** 2).mean(axis=1), 1.0, rtol=1e-12)
+
+
+def test_rmsnorm_power_of_two_scaling_invariance():
+    # mean of squares scales by 4^k, so the output is unchanged (eps 1e-20 is
+    # far below binary64 resolution here)
+    v = rng(62).normal(0, 1, (3, 256))
+    g = rng(63).uniform(0.5, 2.0, 256).astype(np.float32)
+    a = oracle.hc_rmsnorm(bf16_of(v), g)[1]
+    b = oracle.hc_rmsnorm(bf16_of(v * 8.0), g)[1]
+    c = oracle.hc_rmsnorm(bf16_of(v / 64.0), g)[1]
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def test_rmsnorm_is_linear_in_the_weight_and_per_channel():
+    v = bf16_of(rng(64).normal(0, 1, (2, 128)))
+    g = rng(65).uniform(0.5, 2.0, 128).astype(np.float32)
+    base, _ = oracle.hc_rmsnorm(v, g)
+    twice, _ = oracle.hc_rmsnorm(v, (2.0 * g).astype(np.float32))
+    np.testing.assert_array_equal(twice, 2.0 * base)
+    # a weight of zero on one channel zeroes exactly that channel
+    g0 = g.copy()
+    g0[17] = 0.0
+    z, _ = oracle.hc_rmsnorm(v, g0)
+    assert np.all(z[:, 17] == 0.0)
+    np.testing.assert_array_equal(np.delete(z, 17, axis=1), np.delete(base, 17, axis=1))
+
+
+def test_rmsnorm_normalises_each_token_separately():
+    v = rng(66).normal(0, 1, (2, 64))
+    both, _ = oracle.hc_rmsnorm(bf16_of(np.stack([v[0], 1000 * v[1]])), np.ones(64, np.float32))
+    one, _ = oracle.hc_rmsnorm(bf16_of(v[:1]), np.ones(64, np.float32))
+    np.testing.assert_array_equal(both[0], one[0])
+
+
+def test_rmsnorm_zero_row_and_eps():
+    z = np.zeros((1, 32), np.uint16)
+    out, bits = oracle.hc_rmsnorm(z, np.ones(32, np.float32))
+    assert np.all(out == 0.0) and np.all(bits == 0)
+    # a tiny row meets eps: y = 2^-60 everywhere, eps = 2^-100 * 3 ->
+    # out = 2^-60 / sqrt(2^-120 + 3 * 2^-100) = 2^-60 / (2^-50 sqrt(3 + 2^-20))
+    y = bf16_of(np.full((1, 32), 2.0 ** -60))
+    out, _ = oracle.hc_rmsnorm(y, np.ones(32, np.float32), eps=3 * 2.0 ** -100)
+    np.testing.assert_allclose(out, 2.0 ** -10 / math.sqrt(3 + 2.0 ** -20), rtol=1e-14)
