@@ -139,7 +139,26 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps,
                        uint16_t *y, void *workspace, size_t workspace_bytes,
                        hc_stream_t stream);
 
-/* Scratch bytes hc_mixes_pre may need for these sizes when mixes is NULL
+/*
+ * hc_mixes_pre_norm -- hc_mixes_pre whose collapsed output is also passed
+ * through the RMSNorm the block applies before the sublayer (attn_norm /
+ * ffn_norm; named on the pages but not shown, so the standard form is
+ * taken): with yc the bf16 collapse of hc_mixes_pre,
+ *   y[t][c] = bf16( (yc[t][c] / sqrt(mean_c yc[t][c]^2 + rms_eps)) * rms_weight[c] ).
+ *   rms_weight [d] float (in, 16-byte aligned); rms_eps >= 0 (the model uses
+ *   1e-20); all other arguments, the workspace rule included, as in
+ *   hc_mixes_pre.  y holds the normalised rows; pre/post/comb/mixes are those
+ *   of hc_mixes_pre.  rms_weight == NULL is HC_ERR_INVALID_ARG.
+ */
+hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
+                            float norm_eps, const uint16_t *x, const float *w_mix,
+                            const float *hc_scale, const float *hc_base,
+                            const float *rms_weight, float rms_eps, float *mixes,
+                            float *pre, float *post, float *comb, uint16_t *y,
+                            void *workspace, size_t workspace_bytes,
+                            hc_stream_t stream);
+
+/* Scratch bytes hc_mixes_pre(_norm) may need for these sizes when mixes is NULL
  * (n * mix_hc floats, rounded up to 256 bytes; 0 for n == 0 or invalid
  * sizes).  Pure host function; the value depends only on its arguments. */
 size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);

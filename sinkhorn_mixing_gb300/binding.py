@@ -50,6 +50,8 @@ def lib():
         L.hc_post.argtypes = [i64, i32, i64, P, P, P, P, P, P]
         L.hc_mixes_pre.argtypes = [i64, i32, i64, i32, f32, f32, P, P, P, P, P, P, P, P, P, P,
                                    ctypes.c_size_t, P]
+        L.hc_mixes_pre_norm.argtypes = [i64, i32, i64, i32, f32, f32, P, P, P, P, P, f32, P, P,
+                                        P, P, P, P, ctypes.c_size_t, P]
         L.hc_workspace_bytes.argtypes = [i64, i32, i64]
         L.hc_workspace_bytes.restype = ctypes.c_size_t
         L.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -57,7 +59,7 @@ def lib():
         L.hc_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
         L.hc_selftest_wait_timeout.restype = i32
         for f in ("hc_mixes", "hc_split_sinkhorn", "hc_pre", "hc_post", "hc_mixes_pre",
-                  "hc_device_error"):
+                  "hc_mixes_pre_norm", "hc_device_error"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -254,6 +256,45 @@ def hc_mixes_pre(x, w_mix, hc_scale, hc_base, sinkhorn_iters: int = 20, eps: flo
                                   _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
                                   _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb), _ptr(y),
                                   _ptr(workspace), wbytes, _stream(dev, stream)), "hc_mixes_pre")
+    return y, pre, post, comb, mixes
+
+
+def hc_mixes_pre_norm(x, w_mix, hc_scale, hc_base, rms_weight, sinkhorn_iters: int = 20,
+                      eps: float = 1e-6, norm_eps: float = 1e-20, rms_eps: float = 1e-20,
+                      want_mixes: bool = False, mixes=None, pre=None, post=None, comb=None, y=None,
+                      workspace=None, stream=None):
+    """hc_mixes_pre whose collapsed output y is also RMS-normalised with
+    rms_weight [d].  Returns (y, pre, post, comb, mixes-or-None)."""
+    _need(x, "x", torch.bfloat16)
+    dev = x.device
+    lead, n, hc, d = _stream_dims(x)
+    mix = (2 + hc) * hc
+    _need(w_mix, "w_mix", torch.float32, dev)
+    _need(hc_scale, "hc_scale", torch.float32, dev)
+    _need(hc_base, "hc_base", torch.float32, dev)
+    _need(rms_weight, "rms_weight", torch.float32, dev)
+    if tuple(rms_weight.shape) != (d,):
+        raise ValueError("rms_weight must have shape (%d,)" % d)
+    if want_mixes or mixes is not None:
+        mixes = _out(mixes, "mixes", lead + (mix,), torch.float32, dev)
+    pre = _out(pre, "pre", lead + (hc,), torch.float32, dev)
+    post = _out(post, "post", lead + (hc,), torch.float32, dev)
+    comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
+    y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
+    wbytes = 0
+    if mixes is None:
+        wbytes = hc_workspace_bytes(n, hc, d)
+        if workspace is None and wbytes:
+            workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev)
+        wbytes = workspace.numel()
+    with _on_device(dev):
+        _check(lib().hc_mixes_pre_norm(n, hc, d, int(sinkhorn_iters), float(eps), float(norm_eps),
+                                       _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
+                                       _ptr(rms_weight), float(rms_eps), _ptr(mixes), _ptr(pre),
+                                       _ptr(post), _ptr(comb), _ptr(y), _ptr(workspace), wbytes,
+                                       _stream(dev, stream)), "hc_mixes_pre_norm")
     return y, pre, post, comb, mixes
 
 

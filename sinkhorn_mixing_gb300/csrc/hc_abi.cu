@@ -248,23 +248,29 @@ hc_status hc_post(int64_t n, int hc, int64_t d, const uint16_t *out, const uint1
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
-hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
-                       const uint16_t *x, const float *w_mix, const float *hc_scale,
-                       const float *hc_base, float *mixes, float *pre, float *post, float *comb,
-                       uint16_t *y, void *workspace, size_t workspace_bytes,
-                       hc_stream_t stream) {
+namespace {
+
+// hc_mixes_pre, and hc_mixes_pre_norm when rms_w is not null.
+hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                         const uint16_t *x, const float *w_mix, const float *hc_scale,
+                         const float *hc_base, const float *rms_w, float rms_eps, float *mixes,
+                         float *pre, float *post, float *comb, uint16_t *y, void *workspace,
+                         size_t workspace_bytes, hc_stream_t stream) {
     hc_status st = check_shape(n, hc, d);
     if (st != HC_OK) return st;
     if (iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (rms_w != nullptr && !finite_nonneg(rms_eps)) return HC_ERR_INVALID_ARG;
     if (n == 0) return HC_OK;
     if ((st = ptrs_ok({x, w_mix, hc_scale, hc_base, pre, post, comb, y})) != HC_OK) return st;
+    if (rms_w != nullptr && !al16(rms_w)) return HC_ERR_MISALIGNED;
     if (mixes != nullptr && !al16(mixes)) return HC_ERR_MISALIGNED;
     const uint64_t mix = (uint64_t)(2 + hc) * hc, F = (uint64_t)hc * d;
     const Range rmix = mixes ? rng(mixes, n * mix * 4) : Range{0, 0};
+    const Range rrms = rms_w ? rng(rms_w, (uint64_t)d * 4) : Range{0, 0};
     if (!disjoint({rmix, rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
                    rng(comb, n * (uint64_t)hc * hc * 4ull), rng(y, (uint64_t)n * d * 2)},
                   {rng(x, n * F * 2), rng(w_mix, mix * F * 4), rng(hc_scale, 12),
-                   rng(hc_base, mix * 4)}))
+                   rng(hc_base, mix * 4), rrms}))
         return HC_ERR_INVALID_ARG;
     // Without `mixes` the workspace must be there (the general path keeps
     // the mix numbers in it between its stages).
@@ -278,27 +284,56 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float
         if (!disjoint({rw}, {rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
                              rng(comb, n * (uint64_t)hc * hc * 4ull),
                              rng(y, (uint64_t)n * d * 2), rng(x, n * F * 2),
-                             rng(w_mix, mix * F * 4), rng(hc_scale, 12), rng(hc_base, mix * 4)}))
+                             rng(w_mix, mix * F * 4), rng(hc_scale, 12), rng(hc_base, mix * 4),
+                             rrms}))
             return HC_ERR_INVALID_ARG;
     }
     hc::DeviceInfo di;
     if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (hc::decode_supported(n, hc, d, di)) {
-        return from_cuda(hc::launch_decode(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
-                                           hc_base, mixes, pre, post, comb, y, di, s));
-    }
-    if (hc::fused_supported(hc, d, di)) {
-        return from_cuda(hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
-                                          hc_base, mixes, pre, post, comb, y, di, s));
+    if (rms_w == nullptr) {
+        if (hc::decode_supported(n, hc, d, di)) {
+            return from_cuda(hc::launch_decode(n, hc, d, iters, eps, norm_eps, x, w_mix,
+                                               hc_scale, hc_base, mixes, pre, post, comb, y, di,
+                                               s));
+        }
+        if (hc::fused_supported(hc, d, di)) {
+            return from_cuda(hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix,
+                                              hc_scale, hc_base, mixes, pre, post, comb, y, di,
+                                              s));
+        }
     }
     // General path: three kernels, the mix numbers passing through m.
     cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, m, di, s);
     if (e == cudaSuccess)
         e = hc::launch_split_sinkhorn(n, hc, iters, eps, m, hc_scale, hc_base, pre, post, comb,
                                       di, s);
-    if (e == cudaSuccess) e = hc::launch_pre(n, hc, d, x, pre, y, di, s);
+    if (e == cudaSuccess)
+        e = rms_w == nullptr ? hc::launch_pre(n, hc, d, x, pre, y, di, s)
+                             : hc::launch_pre_norm(n, hc, d, x, pre, rms_w, rms_eps, y, di, s);
     return from_cuda(e);
+}
+
+}  // namespace
+
+hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                       const uint16_t *x, const float *w_mix, const float *hc_scale,
+                       const float *hc_base, float *mixes, float *pre, float *post, float *comb,
+                       uint16_t *y, void *workspace, size_t workspace_bytes,
+                       hc_stream_t stream) {
+    return mixes_pre_impl(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale, hc_base, nullptr,
+                          0.0f, mixes, pre, post, comb, y, workspace, workspace_bytes, stream);
+}
+
+hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                            const uint16_t *x, const float *w_mix, const float *hc_scale,
+                            const float *hc_base, const float *rms_weight, float rms_eps,
+                            float *mixes, float *pre, float *post, float *comb, uint16_t *y,
+                            void *workspace, size_t workspace_bytes, hc_stream_t stream) {
+    if (rms_weight == nullptr) return HC_ERR_INVALID_ARG;
+    return mixes_pre_impl(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale, hc_base,
+                          rms_weight, rms_eps, mixes, pre, post, comb, y, workspace,
+                          workspace_bytes, stream);
 }
 
 hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream) {

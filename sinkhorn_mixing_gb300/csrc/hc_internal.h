@@ -61,6 +61,12 @@ cudaError_t launch_split_sinkhorn(int64_t n, int hc, int iters, float eps, const
 cudaError_t launch_pre(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
                        uint16_t *y, const DeviceInfo &di, cudaStream_t s);
 
+// Collapse + RMSNorm (out_c = y_c / sqrt(mean(y^2) + eps) * g_c), one CTA
+// per token.
+cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
+                            const float *g, float eps, uint16_t *y, const DeviceInfo &di,
+                            cudaStream_t s);
+
 cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
                         const uint16_t *res, const float *post, const float *comb, uint16_t *y,
                         const DeviceInfo &di, cudaStream_t s);
