@@ -184,7 +184,7 @@ hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t 
     if (hc::decode_supported(n, hc, d, di)) {
         return from_cuda(hc::launch_decode(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
                                            w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
-                                           nullptr, nullptr, di, s));
+                                           nullptr, nullptr, nullptr, 0.0f, di, s));
     }
     if (hc::fused_supported(hc, d, di)) {
         return from_cuda(hc::launch_fused(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
@@ -291,17 +291,21 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
     hc::DeviceInfo di;
     if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (rms_w == nullptr) {
-        if (hc::decode_supported(n, hc, d, di)) {
-            return from_cuda(hc::launch_decode(n, hc, d, iters, eps, norm_eps, x, w_mix,
-                                               hc_scale, hc_base, mixes, pre, post, comb, y, di,
-                                               s));
-        }
-        if (hc::fused_supported(hc, d, di)) {
-            return from_cuda(hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix,
-                                              hc_scale, hc_base, mixes, pre, post, comb, y, di,
-                                              s));
-        }
+    if (hc::decode_supported(n, hc, d, di)) {
+        return from_cuda(hc::launch_decode(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
+                                           hc_base, mixes, pre, post, comb, y, rms_w, rms_eps,
+                                           di, s));
+    }
+    if (hc::fused_supported(hc, d, di)) {
+        // With the RMSNorm: the fused kernel, then one pass over its rows.  A
+        // second pass inside the fused kernel lengthened the chain that bounds
+        // it (1.33 ms against 0.69 ms at 65,536 tokens, d = 5120); the
+        // separate pass moves 2 x 10 KB per token.
+        cudaError_t e = hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
+                                         hc_base, mixes, pre, post, comb, y, di, s);
+        if (e == cudaSuccess && rms_w != nullptr)
+            e = hc::launch_rmsnorm(n, d, y, rms_w, rms_eps, di, s);
+        return from_cuda(e);
     }
     // General path: three kernels, the mix numbers passing through m.
     cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, m, di, s);

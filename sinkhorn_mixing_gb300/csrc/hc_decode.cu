@@ -74,6 +74,8 @@ struct DecodeParams {
     float *comb;
     uint16_t *y;
     unsigned int *err;
+    const float *rms_w;  // RMSNorm weight of the sublayer input, or null
+    float rms_eps;
 };
 
 __host__ __device__ constexpr int round4(int t) { return (t + 3) & ~3; }
@@ -122,7 +124,7 @@ __host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
 }
 __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
     return wreg_bytes(w) + xreg_bytes(w, tpc) + kCluster * kRecStride * 4 + kMaxTok * 4 * 4 +
-           2 * 8 + 16;
+           kCluster * kMaxTok * 4 + 3 * 8 + 16;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
@@ -134,26 +136,31 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + wreg);  // [round4(tpc)][nf]
     float *recv = reinterpret_cast<float *>(smem + wreg + xreg_bytes(w, p.tpc));  // [16][28]
     float *preb = recv + kCluster * kRecStride;     // [16][4]: pre of the cluster's tokens
-    uint64_t *bars = reinterpret_cast<uint64_t *>(preb + kMaxTok * 4);
-    int *abort_word = reinterpret_cast<int *>(bars + 2);
+    float *normp = preb + kMaxTok * 4;              // [16 senders][16 tokens]: partial sums of y^2
+    uint64_t *bars = reinterpret_cast<uint64_t *>(normp + kCluster * kMaxTok);
+    int *abort_word = reinterpret_cast<int *>(bars + 3);
     volatile int *abort = abort_word;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
     const int64_t tok0 = (int64_t)(blockIdx.x / kCluster) * p.tpc;
     const int tv = (int)((int64_t)p.n - tok0 < p.tpc ? (int64_t)p.n - tok0 : p.tpc);
     const bool mixes_only = p.mixes_only != 0;
-    const uint32_t bRecv = su32(bars), bPre = su32(bars + 1);
+    const uint32_t bRecv = su32(bars), bPre = su32(bars + 1), bNorm = su32(bars + 2);
+    const bool norm = p.rms_w != nullptr && !mixes_only;
     const int64_t F = 4LL * p.d;
 
     // Each barrier completes once: recv when the 16 records of this CTA's
-    // token are in (owners only), pre when pre of all tv tokens is in.
+    // token are in (owners only), pre when pre of all tv tokens is in, norm
+    // (with the RMSNorm) when every CTA's partial sum of y^2 of every token is.
     if (threadIdx.x == 0) {
         *abort_word = 0;
         mbar_init(bRecv, 1);
         mbar_init(bPre, 1);
+        mbar_init(bNorm, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (rank < tv) mbar_expect_tx(bRecv, kCluster * kRecVals * 4);
         if (!mixes_only) mbar_expect_tx(bPre, (uint32_t)tv * 16);
+        if (norm) mbar_expect_tx(bNorm, (uint32_t)(kCluster * tv * 4));
     }
     cluster_arrive();  // waited for before the first remote store
 
@@ -243,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         st_async_f32(mapa(su32(recv + rank * kRecStride + slot), (uint32_t)t), s,
                      mapa(bRecv, (uint32_t)t));
     }
+    __syncthreads();  // the partials are read: their space may take the collapsed rows
 
     if (rank < tv && warp == 0) {
         // Owner of token tok0 + rank: lane k < 25 sums value k of the 16
@@ -287,13 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             }
         }
     } else if (!mixes_only && warp > 0) {
-        // Collapse y = sum_j pre_j x_j of this CTA's channels, warps 1..15.
+        // Collapse y = sum_j pre_j x_j of this CTA's channels, warps 1..15,
+        // one token per warp at a time.  With the RMSNorm the rows are kept
+        // in shared memory (bf16), the warp's partial sum of y^2 goes to every
+        // CTA of the cluster, and the rows are scaled once all 16 are in.
         if (__all_sync(0xFFFFFFFFu, wait_bar<true>(bPre, 0, abort, p.err))) {
             const int xv = w / 8;
+            uint4 *ybuf = reinterpret_cast<uint4 *>(ws);  // [16 tokens][xv]
             for (int t = warp - 1; t < tv; t += kWarps - 1) {
                 const float4 pr = reinterpret_cast<const float4 *>(preb)[t];
                 const uint16_t *xt = xs + t * nf;
                 uint4 *yt = reinterpret_cast<uint4 *>(p.y + (tok0 + t) * (int64_t)p.d + rank * w);
+                float ss = 0.f;
                 for (int q = lane; q < xv; q += 32) {
                     float acc8[8], f8[8];
                     unpack8(reinterpret_cast<const uint4 *>(xt)[q], f8);
@@ -308,7 +321,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
                     unpack8(reinterpret_cast<const uint4 *>(xt + 3 * w)[q], f8);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) acc8[e] = fmaf(pr.w, f8[e], acc8[e]);
-                    st_stream(yt + q, pack8(acc8));
+                    const uint4 yv = pack8(acc8);
+                    if (!norm) {
+                        st_stream(yt + q, yv);
+                    } else {
+                        ybuf[t * xv + q] = yv;
+                        unpack8(yv, f8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(f8[e], f8[e], ss);
+                    }
+                }
+                if (norm) {
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+                    if (lane < kCluster)
+                        st_async_f32(mapa(su32(normp + rank * kMaxTok + t), (uint32_t)lane), ss,
+                                     mapa(bNorm, (uint32_t)lane));
+                }
+            }
+            if (norm &&
+                __all_sync(0xFFFFFFFFu, wait_bar<true>(bNorm, 0, abort, p.err))) {
+                for (int t = warp - 1; t < tv; t += kWarps - 1) {
+                    float tot = 0.f;
+                    for (int s2 = 0; s2 < kCluster; ++s2) tot += normp[s2 * kMaxTok + t];
+                    const float r = rsqrtf(tot / (float)p.d + p.rms_eps);
+                    uint4 *yt =
+                        reinterpret_cast<uint4 *>(p.y + (tok0 + t) * (int64_t)p.d + rank * w);
+                    const float4 *gw = reinterpret_cast<const float4 *>(p.rms_w + rank * w);
+                    for (int q = lane; q < xv; q += 32) {
+                        float f8[8], o8[8];
+                        unpack8(ybuf[t * xv + q], f8);
+                        const float4 g0 = __ldg(gw + 2 * q), g1 = __ldg(gw + 2 * q + 1);
+                        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o8[e] = (f8[e] * r) * gv[e];
+                        st_stream(yt + q, pack8(o8));
+                    }
                 }
             }
         }
@@ -380,7 +429,8 @@ bool decode_supported(int64_t n, int hc, int64_t d, const DeviceInfo &di) {
 cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
                           const uint16_t *x, const float *w, const float *scale,
                           const float *base, float *mixes, float *pre, float *post,
-                          float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+                          float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                          const DeviceInfo &di, cudaStream_t s) {
     const DevState &st = dec_state(di);
     if (!st.ok || hc != 4 || n < 1 || n > (int64_t)kMaxTok * st.max_clusters)
         return cudaErrorNotSupported;
@@ -404,6 +454,8 @@ cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, fl
     p.comb = comb;
     p.y = y;
     p.err = di.err_word;
+    p.rms_w = rms_w;
+    p.rms_eps = rms_eps;
     const int nclusters = (int)((n + p.tpc - 1) / p.tpc);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));

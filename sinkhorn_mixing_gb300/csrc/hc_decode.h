@@ -16,10 +16,12 @@ bool decode_supported(int64_t n, int hc, int64_t d, const DeviceInfo &di);
 
 // pre == nullptr selects the projection-only mode (hc_mixes): only `mixes`
 // is written.  Otherwise pre, post, comb and y are written, and mixes when
-// it is not null.
+// it is not null; with rms_w the collapsed rows are RMS-normalised
+// (y = (yc / sqrt(mean yc^2 + rms_eps)) * rms_w).
 cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
                           const uint16_t *x, const float *w, const float *scale,
                           const float *base, float *mixes, float *pre, float *post,
-                          float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s);
+                          float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                          const DeviceInfo &di, cudaStream_t s);
 
 }  // namespace hc

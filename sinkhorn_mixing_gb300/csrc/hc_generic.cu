@@ -4,6 +4,7 @@
 //   k_split_sinkhorn split + Sinkhorn, one thread per token ("Reading weights")
 //   k_pre            collapse y = sum_j pre_j x_j (Block.hc_pre)
 //   k_pre_norm       the collapse followed by the RMSNorm of the sublayer input
+//   k_rmsnorm        that RMSNorm alone, in place, after the fused kernel
 //   k_post           expansion y_k = post_k out + sum_j comb_jk r_j (Block.hc_post)
 //
 // k_pre and k_post are HBM streams: a warp owns one (token, channel segment)
@@ -318,6 +319,53 @@ __global__ void __launch_bounds__(256) k_pre_norm(int64_t nv, float eps, const u
     }
 }
 
+// --------------------------------------------------------- k_rmsnorm
+// RMSNorm of bf16 rows in place, one CTA per row: each thread keeps its
+// vectors in registers while the mean of squares is reduced in a fixed order,
+// then writes (y * r) * g over them.
+__global__ void __launch_bounds__(256) k_rmsnorm(int64_t nv, float eps, uint4 *__restrict__ y,
+                                                 const float *__restrict__ g) {
+    constexpr int kPer = 4;  // vectors per thread held in registers (nv <= 1024)
+    __shared__ float red[8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint4 *yt = y + (int64_t)blockIdx.x * nv;
+    uint4 v[kPer];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int64_t q = threadIdx.x + (int64_t)k * 256;
+        if (q < nv) {
+            v[k] = yt[q];
+            float f[8];
+            unpack8(v[k], f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float r = rsqrtf(tot / (float)(nv * 8) + eps);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int64_t q = threadIdx.x + (int64_t)k * 256;
+        if (q < nv) {
+            float f[8], o[8];
+            unpack8(v[k], f);
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q);
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q + 1);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
+            st_stream(yt + q, pack8(o));
+        }
+    }
+}
+
 // ------------------------------------------------------ k_post_shared
 // k_post for large hc (8): the token's post and comb live in a per-warp slot
 // of shared memory and are read as broadcasts, instead of 72 registers per
@@ -451,6 +499,13 @@ cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, con
         k_pre_norm<4><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
     else
         k_pre_norm<8><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
+    return launched();
+}
+
+cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
+                           const DeviceInfo &, cudaStream_t s) {
+    if (d / 8 > 4 * 256) return cudaErrorNotSupported;
+    k_rmsnorm<<<(unsigned)n, 256, 0, s>>>(d / 8, eps, reinterpret_cast<uint4 *>(y), g);
     return launched();
 }
 

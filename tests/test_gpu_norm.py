@@ -80,13 +80,14 @@ def test_norm_matches_oracle(hc, n, H, d):
     assert np.mean(key_diff(inputs.bf16_bits(y), want_bits) <= 1) > 0.999
 
 
+@pytest.mark.parametrize("path", ["general", "auto"])
 @pytest.mark.parametrize("n,H,d", [(64, 4, 5120), (300, 8, 1024), (1000, 4, 5120)])
-def test_norm_is_rmsnorm_of_the_same_collapse(hc, n, H, d):
+def test_norm_is_rmsnorm_of_the_same_collapse(hc, n, H, d, path):
     # the same path without the norm gives the collapse the norm was applied
     # to; normalising it in float64 must land within one bf16 step
     x, w, sc, base, rw = case(n, H, d, 17 + H)
     old = os.environ.get("HCMIX_PATH")
-    os.environ["HCMIX_PATH"] = "general"
+    os.environ["HCMIX_PATH"] = path
     try:
         y = hc.hc_mixes_pre_norm(x, w, sc, base, rw)[0]
         yc = hc.hc_mixes_pre(x, w, sc, base)[0]
