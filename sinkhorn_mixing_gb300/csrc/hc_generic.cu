@@ -3,8 +3,6 @@
 //   k_mixes          mix projection + RMS statistic ("Mix projection" page)
 //   k_split_sinkhorn split + Sinkhorn, one thread per token ("Reading weights")
 //   k_pre            collapse y = sum_j pre_j x_j (Block.hc_pre)
-//   k_pre_norm       the collapse followed by the RMSNorm of the sublayer input
-//   k_rmsnorm        that RMSNorm alone, in place, after the fused kernel
 //   k_post           expansion y_k = post_k out + sum_j comb_jk r_j (Block.hc_post)
 //
 // k_pre and k_post are HBM streams: a warp owns one (token, channel segment)
@@ -257,115 +255,6 @@ __global__ void __launch_bounds__(256) k_post(int64_t n, Units un, const uint4 *
     }
 }
 
-// --------------------------------------------------------- k_pre_norm
-// Collapse followed by the RMSNorm of the sublayer input, one CTA per token:
-// the collapse of the whole row (same arithmetic and order as k_pre) is
-// rounded to bf16 and kept in shared memory, the mean of its squares is
-// reduced in a fixed order, and out_c = (y_c * r) * g_c is written, with
-// r = 1/sqrt(mean(y^2) + eps).
-template <int HC>
-__global__ void __launch_bounds__(256) k_pre_norm(int64_t nv, float eps, const uint4 *__restrict__ x,
-                                                  const float *__restrict__ pre,
-                                                  const float *__restrict__ g, uint4 *__restrict__ y) {
-    extern __shared__ uint4 ys[];  // the row's nv collapsed vectors
-    __shared__ float red[8];
-    const int64_t t = blockIdx.x;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float p[HC];
-#pragma unroll
-    for (int q = 0; q < HC / 4; ++q) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(pre + t * HC) + q);
-        p[4 * q] = v.x, p[4 * q + 1] = v.y, p[4 * q + 2] = v.z, p[4 * q + 3] = v.w;
-    }
-    const uint4 *xt = x + t * HC * nv;
-    float ss = 0.f;
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-        uint4 r[HC];
-#pragma unroll
-        for (int j = 0; j < HC; ++j) r[j] = ld_stream(xt + j * nv + v);
-        float acc[8], f[8];
-        unpack8(r[0], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = p[0] * f[e];
-#pragma unroll
-        for (int j = 1; j < HC; ++j) {
-            unpack8(r[j], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(p[j], f[e], acc[e]);
-        }
-        const uint4 yv = pack8(acc);
-        ys[v] = yv;
-        unpack8(yv, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    const float r = rsqrtf(tot / (float)(nv * 8) + eps);
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-        float f[8], o[8];
-        unpack8(ys[v], f);
-        const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v);
-        const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v + 1);
-        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
-        st_stream(y + t * nv + v, pack8(o));
-    }
-}
-
-// --------------------------------------------------------- k_rmsnorm
-// RMSNorm of bf16 rows in place, one CTA per row: each thread keeps its
-// vectors in registers while the mean of squares is reduced in a fixed order,
-// then writes (y * r) * g over them.
-__global__ void __launch_bounds__(256) k_rmsnorm(int64_t nv, float eps, uint4 *__restrict__ y,
-                                                 const float *__restrict__ g) {
-    constexpr int kPer = 4;  // vectors per thread held in registers (nv <= 1024)
-    __shared__ float red[8];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint4 *yt = y + (int64_t)blockIdx.x * nv;
-    uint4 v[kPer];
-    float ss = 0.f;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int64_t q = threadIdx.x + (int64_t)k * 256;
-        if (q < nv) {
-            v[k] = yt[q];
-            float f[8];
-            unpack8(v[k], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    const float r = rsqrtf(tot / (float)(nv * 8) + eps);
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int64_t q = threadIdx.x + (int64_t)k * 256;
-        if (q < nv) {
-            float f[8], o[8];
-            unpack8(v[k], f);
-            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q);
-            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q + 1);
-            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
-            st_stream(yt + q, pack8(o));
-        }
-    }
-}
-
 // ------------------------------------------------------ k_post_shared
 // k_post for large hc (8): the token's post and comb live in a per-warp slot
 // of shared memory and are read as broadcasts, instead of 72 registers per
@@ -479,33 +368,6 @@ cudaError_t launch_pre(int64_t n, int hc, int64_t d, const uint16_t *x, const fl
         k_pre<4, 2><<<grid, 256, 0, s>>>(n, un, xv, pre, yv);
     else
         k_pre<8, 1><<<grid, 256, 0, s>>>(n, un, xv, pre, yv);
-    return launched();
-}
-
-cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
-                            const float *g, float eps, uint16_t *y, const DeviceInfo &,
-                            cudaStream_t s) {
-    const int64_t nv = d / 8;
-    const size_t smem = (size_t)nv * 16;
-    const uint4 *xv = reinterpret_cast<const uint4 *>(x);
-    uint4 *yv = reinterpret_cast<uint4 *>(y);
-    if (smem > 48 * 1024) {
-        const cudaError_t e = hc == 4
-            ? cudaFuncSetAttribute(k_pre_norm<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-            : cudaFuncSetAttribute(k_pre_norm<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    if (hc == 4)
-        k_pre_norm<4><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
-    else
-        k_pre_norm<8><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
-    return launched();
-}
-
-cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
-                           const DeviceInfo &, cudaStream_t s) {
-    if (d / 8 > 4 * 256) return cudaErrorNotSupported;
-    k_rmsnorm<<<(unsigned)n, 256, 0, s>>>(d / 8, eps, reinterpret_cast<uint4 *>(y), g);
     return launched();
 }
 
