@@ -61,13 +61,15 @@ cudaError_t launch_split_sinkhorn(int64_t n, int hc, int iters, float eps, const
 cudaError_t launch_pre(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
                        uint16_t *y, const DeviceInfo &di, cudaStream_t s);
 
-// Collapse + RMSNorm (out_c = y_c / sqrt(mean(y^2) + eps) * g_c), one CTA
-// per token.
+// Collapse + RMSNorm (out_c = y_c / sqrt(mean(y^2) + eps) * g_c), one row
+// per CTA at a time (rows beyond 2^20 taken in a grid stride); the collapsed
+// row is kept in shared memory up to 96 KB, else in y itself.
 cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, const float *pre,
                             const float *g, float eps, uint16_t *y, const DeviceInfo &di,
                             cudaStream_t s);
 
-// RMSNorm of bf16 rows [n][d] in place (d <= 8192), one CTA per row.
+// RMSNorm of bf16 rows [n][d] in place (d <= 8192), one row per CTA at a
+// time (rows beyond 2^20 taken in a grid stride).
 cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
                            const DeviceInfo &di, cudaStream_t s);
 

@@ -16,113 +16,129 @@ namespace hc {
 namespace {
 
 // --------------------------------------------------------- k_pre_norm
-// Collapse followed by the RMSNorm of the sublayer input, one CTA per token:
-// the collapse of the whole row (same arithmetic and order as k_pre) is
-// rounded to bf16 and kept in shared memory, the mean of its squares is
-// reduced in a fixed order, and out_c = (y_c * r) * g_c is written, with
-// r = 1/sqrt(mean(y^2) + eps).
-template <int HC>
-__global__ void __launch_bounds__(256) k_pre_norm(int64_t nv, float eps, const uint4 *__restrict__ x,
+// Collapse followed by the RMSNorm of the sublayer input, one row per CTA at
+// a time: the collapse of the whole row (same arithmetic and order as k_pre)
+// is rounded to bf16 and kept, the mean of its squares is reduced in a fixed
+// order, and out_c = (y_c * r) * g_c is written, with
+// r = 1/sqrt(mean(y^2) + eps).  The collapsed row is kept in shared memory
+// (kSmemRow) or, for rows too wide for it, in the output row itself; either
+// way each thread reads back only the vectors it wrote.
+template <int HC, bool kSmemRow>
+__global__ void __launch_bounds__(256) k_pre_norm(int64_t n, int64_t nv, float eps,
+                                                  const uint4 *__restrict__ x,
                                                   const float *__restrict__ pre,
                                                   const float *__restrict__ g, uint4 *__restrict__ y) {
-    extern __shared__ uint4 ys[];  // the row's nv collapsed vectors
+    extern __shared__ uint4 ys_smem[];  // the row's nv collapsed vectors (kSmemRow)
     __shared__ float red[8];
-    const int64_t t = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float p[HC];
+    for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
+        uint4 *yt = y + t * nv;
+        uint4 *ys = kSmemRow ? ys_smem : yt;
+        float p[HC];
 #pragma unroll
-    for (int q = 0; q < HC / 4; ++q) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(pre + t * HC) + q);
-        p[4 * q] = v.x, p[4 * q + 1] = v.y, p[4 * q + 2] = v.z, p[4 * q + 3] = v.w;
-    }
-    const uint4 *xt = x + t * HC * nv;
-    float ss = 0.f;
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-        uint4 r[HC];
-#pragma unroll
-        for (int j = 0; j < HC; ++j) r[j] = ld_stream(xt + j * nv + v);
-        float acc[8], f[8];
-        unpack8(r[0], f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = p[0] * f[e];
-#pragma unroll
-        for (int j = 1; j < HC; ++j) {
-            unpack8(r[j], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(p[j], f[e], acc[e]);
+        for (int q = 0; q < HC / 4; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(pre + t * HC) + q);
+            p[4 * q] = v.x, p[4 * q + 1] = v.y, p[4 * q + 2] = v.z, p[4 * q + 3] = v.w;
         }
-        const uint4 yv = pack8(acc);
-        ys[v] = yv;
-        unpack8(yv, f);
+        const uint4 *xt = x + t * HC * nv;
+        float ss = 0.f;
+        for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+            uint4 r[HC];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-    }
+            for (int j = 0; j < HC; ++j) r[j] = ld_stream(xt + j * nv + v);
+            float acc[8], f[8];
+            unpack8(r[0], f);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
+            for (int e = 0; e < 8; ++e) acc[e] = p[0] * f[e];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    const float r = rsqrtf(tot / (float)(nv * 8) + eps);
-    for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
-        float f[8], o[8];
-        unpack8(ys[v], f);
-        const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v);
-        const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v + 1);
-        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            for (int j = 1; j < HC; ++j) {
+                unpack8(r[j], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
-        st_stream(y + t * nv + v, pack8(o));
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(p[j], f[e], acc[e]);
+            }
+            const uint4 yv = pack8(acc);
+            ys[v] = yv;
+            unpack8(yv, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        const float r = rsqrtf(tot / (float)(nv * 8) + eps);
+        for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) {
+            float f[8], o[8];
+            unpack8(ys[v], f);
+            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v);
+            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * v + 1);
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
+            st_stream(yt + v, pack8(o));
+        }
+        __syncthreads();  // red[] and the shared row are reused by the next row
     }
 }
 
 // --------------------------------------------------------- k_rmsnorm
-// RMSNorm of bf16 rows in place, one CTA per row: each thread keeps its
-// vectors in registers while the mean of squares is reduced in a fixed order,
-// then writes (y * r) * g over them.
-__global__ void __launch_bounds__(256) k_rmsnorm(int64_t nv, float eps, uint4 *__restrict__ y,
+// RMSNorm of bf16 rows in place, one row per CTA at a time: each thread keeps
+// its vectors in registers while the mean of squares is reduced in a fixed
+// order, then writes (y * r) * g over them.
+__global__ void __launch_bounds__(256) k_rmsnorm(int64_t n, int64_t nv, float eps,
+                                                 uint4 *__restrict__ y,
                                                  const float *__restrict__ g) {
     constexpr int kPer = 4;  // vectors per thread held in registers (nv <= 1024)
     __shared__ float red[8];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint4 *yt = y + (int64_t)blockIdx.x * nv;
-    uint4 v[kPer];
-    float ss = 0.f;
+    for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
+        uint4 *yt = y + t * nv;
+        uint4 v[kPer];
+        float ss = 0.f;
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int64_t q = threadIdx.x + (int64_t)k * 256;
-        if (q < nv) {
-            v[k] = yt[q];
-            float f[8];
-            unpack8(v[k], f);
+        for (int k = 0; k < kPer; ++k) {
+            const int64_t q = threadIdx.x + (int64_t)k * 256;
+            if (q < nv) {
+                v[k] = yt[q];
+                float f[8];
+                unpack8(v[k], f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
         }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    float tot = 0.f;
+        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        if (lane == 0) red[warp] = ss;
+        __syncthreads();
+        float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += red[w];
-    const float r = rsqrtf(tot / (float)(nv * 8) + eps);
+        for (int w = 0; w < 8; ++w) tot += red[w];
+        const float r = rsqrtf(tot / (float)(nv * 8) + eps);
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-        const int64_t q = threadIdx.x + (int64_t)k * 256;
-        if (q < nv) {
-            float f[8], o[8];
-            unpack8(v[k], f);
-            const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q);
-            const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q + 1);
-            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        for (int k = 0; k < kPer; ++k) {
+            const int64_t q = threadIdx.x + (int64_t)k * 256;
+            if (q < nv) {
+                float f[8], o[8];
+                unpack8(v[k], f);
+                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q);
+                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q + 1);
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
-            st_stream(yt + q, pack8(o));
+                for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
+                st_stream(yt + q, pack8(o));
+            }
         }
+        __syncthreads();  // red[] is reused by the next row
     }
 }
+
+// rows per launch grid: one CTA per row up to this many rows, then a stride
+constexpr int64_t kMaxRowGrid = int64_t(1) << 20;
+// collapsed rows up to this size stay in shared memory (two CTAs per SM)
+constexpr size_t kMaxSmemRow = 96 * 1024;
 
 }  // namespace
 
@@ -130,26 +146,37 @@ cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, con
                             const float *g, float eps, uint16_t *y, const DeviceInfo &,
                             cudaStream_t s) {
     const int64_t nv = d / 8;
-    const size_t smem = (size_t)nv * 16;
+    const size_t row = (size_t)nv * 16;
+    const unsigned grid = (unsigned)(n < kMaxRowGrid ? n : kMaxRowGrid);
     const uint4 *xv = reinterpret_cast<const uint4 *>(x);
     uint4 *yv = reinterpret_cast<uint4 *>(y);
-    if (smem > 48 * 1024) {
+    if (row > kMaxSmemRow) {
+        if (hc == 4)
+            k_pre_norm<4, false><<<grid, 256, 0, s>>>(n, nv, eps, xv, pre, g, yv);
+        else
+            k_pre_norm<8, false><<<grid, 256, 0, s>>>(n, nv, eps, xv, pre, g, yv);
+        return launched();
+    }
+    if (row > 48 * 1024) {
         const cudaError_t e = hc == 4
-            ? cudaFuncSetAttribute(k_pre_norm<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-            : cudaFuncSetAttribute(k_pre_norm<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            ? cudaFuncSetAttribute(k_pre_norm<4, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)row)
+            : cudaFuncSetAttribute(k_pre_norm<8, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)row);
         if (e != cudaSuccess) return e;
     }
     if (hc == 4)
-        k_pre_norm<4><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
+        k_pre_norm<4, true><<<grid, 256, row, s>>>(n, nv, eps, xv, pre, g, yv);
     else
-        k_pre_norm<8><<<(unsigned)n, 256, smem, s>>>(nv, eps, xv, pre, g, yv);
+        k_pre_norm<8, true><<<grid, 256, row, s>>>(n, nv, eps, xv, pre, g, yv);
     return launched();
 }
 
 cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
                            const DeviceInfo &, cudaStream_t s) {
     if (d / 8 > 4 * 256) return cudaErrorNotSupported;
-    k_rmsnorm<<<(unsigned)n, 256, 0, s>>>(d / 8, eps, reinterpret_cast<uint4 *>(y), g);
+    const unsigned grid = (unsigned)(n < kMaxRowGrid ? n : kMaxRowGrid);
+    k_rmsnorm<<<grid, 256, 0, s>>>(n, d / 8, eps, reinterpret_cast<uint4 *>(y), g);
     return launched();
 }
 

@@ -127,3 +127,45 @@ def test_norm_deterministic_and_guarded(hc):
     torch.cuda.synchronize()
     assert torch.equal(first.view(torch.int16), y.view(torch.int16))
     assert torch.all(buf[:pad] == 77) and torch.all(buf[-pad:] == 77)
+
+
+def test_norm_wide_rows_kept_in_the_output(hc):
+    # d = 50,176: a collapsed row (98 KB) is too wide for shared memory and is
+    # kept in y between the two passes
+    n, H, d = 3, 4, 50176
+    x, w, sc, base, rw = case(n, H, d, 41)
+    y, pre, post, comb, m = hc.hc_mixes_pre_norm(x, w, sc, base, rw, 20, want_mixes=True)
+    torch.cuda.synchronize()
+    xb = inputs.bf16_bits(x)
+    compare.check_mixes(np64(m), oracle.hc_mixes(xb, w.cpu().numpy()))
+    _, yc_bits, mag = oracle.hc_pre(xb, np64(pre))
+    out_want, want_bits = oracle.hc_rmsnorm(yc_bits, rw.cpu().numpy())
+    yc = oracle.bf16_bits_to_f64(yc_bits)
+    inv = 1.0 / np.sqrt((yc ** 2).mean(axis=1, keepdims=True) + 1e-20)
+    got = oracle.bf16_bits_to_f64(inputs.bf16_bits(y))
+    g = rw.cpu().numpy().astype(np.float64)
+    allowed = (np.abs(g) * inv * (compare.bf16_ulp(yc) + H * 2.0 ** -24 * mag) +
+               compare.bf16_ulp(out_want) + 1e-5 * np.abs(out_want))
+    assert np.all(np.abs(got - out_want) <= allowed)
+    assert np.mean(key_diff(inputs.bf16_bits(y), want_bits) <= 1) > 0.999
+
+
+@pytest.mark.parametrize("d", [8, 1024])
+def test_norm_rows_beyond_one_launch_grid(hc, d):
+    # 2^20 + 5 rows: the norm kernels take one row per CTA up to 2^20 rows and
+    # the rest in a grid stride (d = 8: general path; d = 1024: the fused
+    # kernel followed by the row pass)
+    n, H = (1 << 20) + 5, 4
+    g = torch.Generator(device="cuda").manual_seed(d)
+    x = torch.randn((n, H, d), device="cuda", generator=g, dtype=torch.bfloat16)
+    w = torch.randn(((2 + H) * H, H * d), device="cuda", generator=g) / (H * d) ** 0.5
+    sc = torch.rand(3, device="cuda", generator=g) + 0.5
+    base = torch.randn((2 + H) * H, device="cuda", generator=g)
+    rw = torch.rand(d, device="cuda", generator=g) + 0.25
+    y = hc.hc_mixes_pre_norm(x, w, sc, base, rw)[0]
+    yc = hc.hc_mixes_pre(x, w, sc, base)[0]
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([np.arange(4), np.arange((1 << 20) - 4, n),
+                                    np.random.default_rng(d).integers(0, n, 200)]))
+    _, want = oracle.hc_rmsnorm(inputs.bf16_bits(yc[idx]), rw.cpu().numpy())
+    assert key_diff(inputs.bf16_bits(y[idx]), want).max() <= 1
