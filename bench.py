@@ -53,6 +53,9 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the 64-token decode latency line item")
+    ap.add_argument("--projection", action="store_true",
+                    help="instead of the step: time the mix projection (hc_mixes) on its "
+                         "CUDA-core (FFMA) kernel and on the tensor-core kernels, one JSON line")
     return ap.parse_args(argv)
 
 
@@ -62,6 +65,12 @@ def bytes_mixes_pre(n, hc, d):
     """x read once, y written once, pre/post/comb written once, W read once."""
     mix = (2 + hc) * hc
     return n * (hc * d * 2 + d * 2 + (2 * hc + hc * hc) * 4) + mix * hc * d * 4 + (3 + mix) * 4
+
+
+def bytes_mixes(n, hc, d):
+    """x read once, W read once, the mix numbers written once."""
+    mix = (2 + hc) * hc
+    return n * (hc * d * 2 + mix * 4) + mix * hc * d * 4
 
 
 def bytes_post(n, hc, d):
@@ -392,6 +401,82 @@ def run_reference(args, wl, rank):
 
 # ---------------------------------------------------------------- our arm
 
+def projection_compare(args, wl, dev):
+    """The mix projection (hc_mixes) of the workload on each of its kernels:
+    the CUDA-core kernel (FFMA, fp32 W tiles in shared memory), the tensor-core
+    kernel with W streamed (bf16 hi + lo, tcgen05), and, where the shape takes
+    it, the fused kernel in its projection-only mode (W resident in the
+    cluster's shared memory).  Each path is pinned through HCMIX_PATH, timed
+    with CUDA events over `steps` launches, and compared with the others."""
+    import torch
+    import sinkhorn_mixing_gb300 as hc
+    from sinkhorn_mixing_gb300 import build, inputs
+
+    build.build()
+    n, H, d = (args.tokens or wl.n), wl.hc, wl.d
+    s = shard_streams(wl, n, 0, dev)
+    p = inputs.make_params(wl, device=dev)
+    x = s["x"]
+    mix = (2 + H) * H
+    flush = None
+    if x.numel() * 2 < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    steps = max(1, min(args.steps, 50))
+    peak, peak_kind = peaks()
+    b = bytes_mixes(n, H, d)
+    flop = 2.0 * n * H * d * mix
+    paths = [("ffma", "CUDA cores (FFMA), fp32 W tiles in shared memory"),
+             ("general", "tensor cores (tcgen05), W streamed as bf16 hi + lo")]
+    if H == 4 and d % 1024 == 0 and d <= 5120:
+        paths.append(("fused", "tensor cores (tcgen05), W resident as bf16 hi + lo"))
+    out, res = {}, {}
+    old = os.environ.get("HCMIX_PATH")
+    try:
+        for name, what in paths:
+            os.environ["HCMIX_PATH"] = name
+            m = torch.empty((n, mix), device=dev)
+            for _ in range(max(3, args.warmup)):
+                if flush is not None:
+                    flush.zero_()
+                hc.hc_mixes(x, p["w"], wl.norm_eps, mixes=m)
+            torch.cuda.synchronize(dev)
+            launches0 = hc.hc_launch_count()
+            tot = 0.0
+            for _ in range(steps):
+                if flush is not None:
+                    flush.zero_()
+                a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                hc.hc_mixes(x, p["w"], wl.norm_eps, mixes=m)
+                e.record()
+                torch.cuda.synchronize(dev)
+                tot += a.elapsed_time(e) / 1e3
+            t = tot / steps
+            res[name] = m
+            out[name] = {"what": what, "us_per_launch": 1e6 * t,
+                         "launches_per_call": (hc.hc_launch_count() - launches0) // steps,
+                         "GBps": b / t / 1e9, "frac_of_hbm": b / t / 1e9 / peak,
+                         "TFLOPs": flop / t / 1e12}
+    finally:
+        if old is None:
+            os.environ.pop("HCMIX_PATH", None)
+        else:
+            os.environ["HCMIX_PATH"] = old
+    if hc.hc_device_error(clear=True):
+        raise RuntimeError("device error word set during the projection measurement")
+    ref = res["ffma"].double()
+    scale = ref.abs().clamp(min=1.0)
+    for name in out:
+        out[name]["max_rel_diff_vs_ffma"] = float(((res[name].double() - ref).abs() / scale).max())
+    line = {"projection": out, "workload": DESCR[args.workload] + (
+                "" if n == wl.n else " [token count overridden: %d]" % n),
+            "tokens": n, "hc": H, "d": d, "algorithmic_bytes": b, "flop": flop,
+            "peak_GBps": peak, "peak_kind": peak_kind, "steps": steps,
+            "l2": "flushed between launches" if flush is not None else
+                  "inputs larger than L2, no flush"}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args, wl, ws, rank, local):
     import torch
     import torch.distributed as dist
@@ -525,6 +610,12 @@ def main():
     wl = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl, rank)
+        return
+    if args.projection:
+        import torch
+        torch.cuda.set_device(local)
+        if rank == 0:
+            projection_compare(args, wl, torch.device("cuda", local))
         return
     if ws > 1:
         import torch

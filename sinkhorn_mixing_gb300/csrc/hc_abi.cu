@@ -165,6 +165,10 @@ size_t hc_workspace_bytes(int64_t n, int hc, int64_t d) {
     return (size_t)((b + 255u) / 256u * 256u);
 }
 
+// Token count from which hc_mixes takes the streamed-W tensor-core kernel
+// rather than the fused kernel's projection-only mode (d = 1024..5120).
+constexpr int64_t kFusedProjectionTokens = 16384;
+
 hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
                    const float *w_mix, float *mixes, hc_stream_t stream) {
     hc_status st = check_shape(n, hc, d);
@@ -186,7 +190,14 @@ hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t 
                                            w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
                                            nullptr, nullptr, nullptr, 0.0f, di, s));
     }
-    if (hc::fused_supported(hc, d, di)) {
+    // The projection alone: the fused kernel (W resident in its clusters'
+    // shared memory, 112 SMs) up to kFusedProjectionTokens; past one wave of
+    // 128-token units the tensor-core kernel with W streamed, on every SM, is
+    // faster (65,536 tokens, d = 5120: 515 against 608 us).  The fused
+    // kernel's gain is its collapse, which the projection alone does not have.
+    if (hc::fused_supported(hc, d, di) &&
+        (n < kFusedProjectionTokens || hc::forced_path() == hc::kPathFused ||
+         !hc::mixtc_supported(hc, d, di))) {
         return from_cuda(hc::launch_fused(n, hc, d, /*iters=*/1, /*eps=*/0.0f, norm_eps, x,
                                           w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
                                           nullptr, nullptr, di, s));

@@ -102,3 +102,21 @@ def test_hc8_mixes_pre_through_tensor_projection(hc, path):
     compare.check_abs(np64(comb), o_comb, 1e-5, "comb")
     want, _, mag = oracle.hc_pre(xb, np64(pre))
     compare.check_bf16(inputs.bf16_bits(y), want, mag, 8, "y")
+
+
+@pytest.mark.parametrize("n", [4096, 16384, 20000])
+def test_projection_only_dispatch_by_token_count(hc, path, n):
+    # hc_mixes alone takes the fused kernel below 16,384 tokens and the
+    # streamed-W tensor-core kernel from there on; both agree with the oracle
+    H, d = 4, 1024
+    x, w = case(n, H, d, 11 + n)
+    path(None)
+    auto = hc.hc_mixes(x, w)
+    path("fused" if n < 16384 else "general")
+    pinned = hc.hc_mixes(x, w)
+    torch.cuda.synchronize()
+    assert torch.equal(auto.view(torch.int32), pinned.view(torch.int32))
+    idx = np.unique(np.concatenate([np.arange(4), np.arange(n - 4, n),
+                                    np.random.default_rng(n).integers(0, n, 200)]))
+    compare.check_mixes(np64(auto)[idx], oracle.hc_mixes(inputs.bf16_bits(x[idx]),
+                                                         w.cpu().numpy()))
