@@ -1,0 +1,277 @@
+"""A model of the synchronisation protocol of the fused hc=4 kernel
+(sinkhorn_mixing_gb300/csrc/hc_fused.cu), run under random interleavings.
+
+Test infrastructure only: it restates the kernel's barriers and roles in
+plain Python and shares no code with the kernel.  Each CTA of a cluster runs
+the kernel's roles as generators that yield the barrier waits they make:
+
+  producer  per tile, waits for the collapse to be at most `lag` tiles
+            behind, then for each stage waits for an empty ring slot, arms
+            its full barrier and issues a load that lands later;
+  mma       per tile, waits for a free accumulator, consumes every stage in
+            order and releases each slot by a commit (commits complete in
+            issue order), then commits acc_full;
+  sq (x4)   consume every stage in order, release it, publish the tile's sums
+            of squares through sq_full / sq_empty;
+  epi (x2)  read the accumulator and the squares, wait until the previous
+            tile's records were read (recv_free), then send their records to
+            the owners, whose recv_full they complete by bytes;
+  owner     waits for its records, reads them, stages pre and signals
+            pre_ready, re-arms recv_full, then releases the record buffer to
+            every sender;
+  collapse  (x2) waits for pre, reads the staging slot, signals col_done.
+
+Up to three randomly chosen roles run a hundred times slower than the rest,
+so that single slow roles fall far behind and early-reuse windows are
+reached.
+
+mbarrier model: a phase completes when its pending arrivals and its
+transaction bytes both reach zero; try_wait(parity) is true iff the current
+phase's parity differs from `parity`, so only the current and the previous
+phase can be told apart, as on the hardware.
+
+Checks: a load never lands in a slot that is being read; every consumer
+finds the stage it expects; an accumulator, a staging slot or a record buffer
+is never overwritten while read; no arrival or byte count underflows; and
+every role finishes (no deadlock).
+"""
+import random
+
+
+class ProtocolError(Exception):
+    pass
+
+
+class Barrier:
+    def __init__(self, name, count):
+        self.name, self.count, self.pending, self.tx, self.completed = name, count, count, 0, 0
+
+    def arrive(self):
+        if self.pending == 0:
+            raise ProtocolError("arrival underflow on " + self.name)
+        self.pending -= 1
+        self._settle()
+
+    def expect_tx(self, n):
+        self.tx += n
+        self.arrive()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        if self.tx < 0 and self.pending == 0:
+            raise ProtocolError("byte count underflow on " + self.name)
+        self._settle()
+
+    def _settle(self):
+        if self.pending == 0 and self.tx == 0:
+            self.completed += 1
+            self.pending = self.count
+
+    def try_wait(self, parity):
+        return parity != (self.completed & 1)
+
+
+def wait(bar, parity):
+    return ("wait", bar, parity)
+
+
+STEP = ("step",)
+
+
+def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_only=False,
+             seed=0, mutation=None):
+    """Run one random interleaving; raises ProtocolError on any violation.
+    `mutation` plants a known protocol mistake (for the tests that show the
+    model can fail): "release_before_read", "empty_parity"."""
+    rnd = random.Random(seed)
+    events = []
+
+    def later(fn):
+        events.append(fn)
+
+    C, T, NS, S = ctas, tiles, stages_per_tile, slots
+    cs = []
+    for r in range(C):
+        cs.append(dict(
+            full=[Barrier("full", 1) for _ in range(S)],
+            empty=[Barrier("empty", 5) for _ in range(S)],  # MMA commit + 4 square warps
+            slot=[None] * S, holders=[set() for _ in range(S)],
+            acc_full=[Barrier("acc_full", 1) for _ in range(2)],
+            acc_empty=[Barrier("acc_empty", 2) for _ in range(2)],
+            acc=[None, None], acc_readers=[0, 0],
+            sq_full=[Barrier("sq_full", 4) for _ in range(2)],
+            sq_empty=[Barrier("sq_empty", 2) for _ in range(2)],
+            sq=[[None] * 4, [None] * 4],
+            recv_full=Barrier("recv_full", 1), recv_free=Barrier("recv_free", C),
+            recv=[None] * C, reading=[False],
+            pre_ready=[Barrier("pre_ready", 1) for _ in range(bufs)],
+            col_done=[Barrier("col_done", 2) for _ in range(bufs)],
+            stage=[None] * bufs, stage_readers=[0] * bufs))
+    for c in cs:
+        c["recv_full"].expect_tx(C)  # one record per sender and round
+
+    def producer(c):
+        for it in range(T):
+            if not mixes_only and it >= lag:
+                tw = it - lag
+                yield wait(c["col_done"][tw % bufs], (tw // bufs) & 1)
+            for st in range(NS):
+                q = NS * it + st
+                s, use = q % S, q // S
+                par = (use & 1) if mutation == "empty_parity" else (use & 1) ^ 1
+                yield wait(c["empty"][s], par)
+                c["full"][s].expect_tx(1)
+
+                def land(c=c, s=s, q=q):
+                    if c["holders"][s]:
+                        raise ProtocolError("a load lands in a slot that is being read")
+                    c["slot"][s] = q
+                    c["full"][s].complete_tx(1)
+                later(land)
+
+    def mma(c):
+        chain = []
+
+        def commit():
+            kind, a, b = chain.pop(0)
+            if kind == "empty":
+                c["holders"][a].discard("mma")
+                c["empty"][a].arrive()
+            else:
+                c["acc"][a] = b
+                c["acc_full"][a].arrive()
+        for it in range(T):
+            b = it & 1
+            yield wait(c["acc_empty"][b], ((it >> 1) & 1) ^ 1)
+            if c["acc_readers"][b]:
+                raise ProtocolError("the MMA overwrites an accumulator being read")
+            for st in range(NS):
+                q = NS * it + st
+                s = q % S
+                yield wait(c["full"][s], (q // S) & 1)
+                if c["slot"][s] != q:
+                    raise ProtocolError("MMA wants stage %d, slot holds %s" % (q, c["slot"][s]))
+                c["holders"][s].add("mma")
+                chain.append(("empty", s, None))
+                later(commit)
+            chain.append(("acc", b, it))
+            later(commit)
+
+    def sq(c, w):
+        for it in range(T):
+            b = it & 1
+            for st in range(NS):
+                q = NS * it + st
+                s = q % S
+                yield wait(c["full"][s], (q // S) & 1)
+                if c["slot"][s] != q:
+                    raise ProtocolError("squares want stage %d, slot holds %s" % (q, c["slot"][s]))
+                c["holders"][s].add(w)
+                yield STEP
+                c["holders"][s].discard(w)
+                c["empty"][s].arrive()
+            yield wait(c["sq_empty"][b], ((it >> 1) & 1) ^ 1)
+            c["sq"][b][w] = it
+            c["sq_full"][b].arrive()
+
+    def epi(c, rank, half):
+        mine = range(half * C // 2, (half + 1) * C // 2) if C > 1 else range(1)
+        for it in range(T):
+            b = it & 1
+            yield wait(c["acc_full"][b], (it >> 1) & 1)
+            if c["acc"][b] != it:
+                raise ProtocolError("read-out finds the accumulator of %s" % c["acc"][b])
+            c["acc_readers"][b] += 1
+            yield STEP
+            c["acc_readers"][b] -= 1
+            c["acc_empty"][b].arrive()
+            yield wait(c["sq_full"][b], (it >> 1) & 1)
+            if c["sq"][b] != [it] * 4:
+                raise ProtocolError("read-out finds squares %s" % c["sq"][b])
+            c["sq_empty"][b].arrive()
+            yield wait(c["recv_free"], (it & 1) ^ 1)
+            for o in mine:
+                def deliver(o=o, it=it):
+                    oc = cs[o]
+                    if oc["reading"][0]:
+                        raise ProtocolError("a record lands while its owner reads")
+                    if oc["recv"][rank] is not None:
+                        raise ProtocolError("a record overwrites an unread one")
+                    oc["recv"][rank] = it
+                    oc["recv_full"].complete_tx(1)
+                later(deliver)
+
+    def owner(c):
+        for it in range(T):
+            yield wait(c["recv_full"], it & 1)
+            if c["recv"] != [it] * C:
+                raise ProtocolError("owner of tile %d finds records %s" % (it, c["recv"]))
+            if mutation == "release_before_read":
+                for d in cs:
+                    later(lambda d=d: d["recv_free"].arrive())
+            c["reading"][0] = True
+            yield STEP
+            c["reading"][0] = False
+            if not mixes_only:
+                i = it % bufs
+                if c["stage_readers"][i]:
+                    raise ProtocolError("pre staging overwritten while the collapse reads it")
+                c["stage"][i] = it
+                c["pre_ready"][i].arrive()
+            c["recv"] = [None] * C
+            c["recv_full"].expect_tx(C)
+            if mutation != "release_before_read":
+                for d in cs:
+                    later(lambda d=d: d["recv_free"].arrive())
+
+    def collapse(c):
+        for it in range(T):
+            i = it % bufs
+            yield wait(c["pre_ready"][i], (it // bufs) & 1)
+            if c["stage"][i] != it:
+                raise ProtocolError("collapse of tile %d reads the pre of %s" % (it, c["stage"][i]))
+            c["stage_readers"][i] += 1
+            yield STEP
+            c["stage_readers"][i] -= 1
+            c["col_done"][i].arrive()
+
+    roles = []
+    for r, c in enumerate(cs):
+        roles += [producer(c), mma(c), owner(c)] + [sq(c, w) for w in range(4)]
+        roles += [epi(c, r, h) for h in range(2)]
+        if not mixes_only:
+            roles += [collapse(c), collapse(c)]
+    # Adversarial schedule: zero to three roles, chosen at random, run a
+    # hundred times slower than the rest, so that one slow consumer or
+    # producer falls far behind and the windows in which a buffer could be
+    # reused early, or a barrier phase be passed twice, are actually reached.
+    speed = [1.0] * len(roles)
+    for k in rnd.sample(range(len(roles)), rnd.choice((0, 1, 2, 3))):
+        speed[k] = 0.01
+    state = [None] * len(roles)
+    live = set()
+    for k, g in enumerate(roles):
+        try:
+            state[k] = next(g)
+            live.add(k)
+        except StopIteration:
+            pass
+    while live or events:
+        ready = [k for k in live if state[k] is STEP or state[k][1].try_wait(state[k][2])]
+        if not ready and not events:
+            raise ProtocolError("deadlock: %d roles wait forever" % len(live))
+        wsum = sum(speed[k] for k in ready) + len(events)
+        x = rnd.random() * wsum
+        k = None
+        for j in ready:
+            x -= speed[j]
+            if x < 0:
+                k = j
+                break
+        if k is not None:
+            try:
+                state[k] = next(roles[k])
+            except StopIteration:
+                live.discard(k)
+        else:
+            events.pop(rnd.randrange(len(events)))()
