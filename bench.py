@@ -172,16 +172,17 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel):
+def traffic_record(kernel, hc, d, n):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the kernel source changed since the counters were taken."""
+    when it was taken on another workload (hc, d, token count) or the kernel
+    source changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         j = json.load(f)
     rec = j.get(kernel)
-    if not rec:
+    if not rec or (rec.get("hc"), rec.get("d"), rec.get("tokens")) != (hc, d, n):
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src):
@@ -565,7 +566,7 @@ def run_ours(args, wl, ws, rank, local):
     dom_is_post = a2 >= a1
     kname = "hc_post" if dom_is_post else "hc_mixes_pre"
     achieved = (b2 / a2 if dom_is_post else b1 / a1) / 1e9
-    tr = traffic_record(kname)
+    tr = traffic_record(kname, H, d, n)
     line = {
         "metric": METRIC, "value": job_tokens_per_s(ws, n, args.steps, tot), "unit": UNIT,
         "n_gpus": ws,

@@ -84,3 +84,21 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = bench.parse(["--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"])
     bench.run_reference(args, inputs.WORKLOADS["tiny"], rank=1)
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_record_only_for_its_workload_and_source(tmp_path, monkeypatch):
+    # the committed DRAM traffic belongs to the large hc=4 workload and to the
+    # kernel source it was captured on; any other workload or an edited
+    # source reports no traffic
+    rec = bench.traffic_record("hc_post", 4, 5120, 65536)
+    assert rec is not None and rec["dram_bytes_per_launch"] > 0
+    assert bench.traffic_record("hc_post", 8, 5120, 65536) is None
+    assert bench.traffic_record("hc_mixes_pre", 4, 5120, 16384) is None
+    assert bench.traffic_record("hc_mixes_pre", 4, 2048, 65536) is None
+    src = tmp_path / "k.cu"
+    src.write_text("a")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"hc_post": dict(
+        rec, source="k.cu")}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_record("hc_post", 4, 5120, 65536) is None
