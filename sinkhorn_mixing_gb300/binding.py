@@ -12,6 +12,7 @@ views ``[b, s, ...]`` tensors as ``[n, ...]``; outputs keep the caller's
 leading dimensions.
 """
 import ctypes
+import functools
 import os
 from typing import Optional
 
@@ -75,7 +76,8 @@ def _check(status: int, what: str):
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int (or None for NULL): ctypes converts it for c_void_p arguments
+    return None if t is None else t.data_ptr()
 
 
 # The raw handle of the current stream without building a Stream object
@@ -83,32 +85,25 @@ def _ptr(t: Optional[torch.Tensor]):
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _stream(dev: torch.device, stream) -> ctypes.c_void_p:
+def _stream(dev: torch.device, stream) -> int:
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
+        return stream.cuda_stream
     if _raw_stream is not None:
-        return ctypes.c_void_p(_raw_stream(dev.index))
-    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        return _raw_stream(dev.index)
+    return torch.cuda.current_stream(dev).cuda_stream
 
 
-class _on_device:
-    """Makes `dev` the current device for the call, switching only when it
-    is not already current."""
-
-    def __init__(self, dev: torch.device):
-        self.idx = dev.index
-        self.prev = None
-
-    def __enter__(self):
-        cur = torch.cuda.current_device()
-        if cur != self.idx:
-            self.prev = cur
-            torch.cuda.set_device(self.idx)
-
-    def __exit__(self, *exc):
-        if self.prev is not None:
-            torch.cuda.set_device(self.prev)
-        return False
+def _call(dev: torch.device, fn, *args):
+    """fn(*args) with `dev` as the current device, switching (and back) only
+    when it is not already current."""
+    cur = torch.cuda.current_device()
+    if cur == dev.index:
+        return fn(*args)
+    torch.cuda.set_device(dev.index)
+    try:
+        return fn(*args)
+    finally:
+        torch.cuda.set_device(cur)
 
 
 def _need(t: torch.Tensor, name: str, dtype, dev=None):
@@ -149,7 +144,9 @@ def abi_version() -> int:
     return int(lib().hc_abi_version())
 
 
+@functools.lru_cache(maxsize=256)
 def hc_workspace_bytes(n: int, hc: int, d: int) -> int:
+    # a pure function of its arguments (hcmix.h), so it is asked once per shape
     return int(lib().hc_workspace_bytes(int(n), int(hc), int(d)))
 
 
@@ -161,9 +158,8 @@ def hc_mixes(x, w_mix, norm_eps: float = 1e-20, mixes=None, stream=None):
     _need(w_mix, "w_mix", torch.float32, dev)
     mix = (2 + hc) * hc
     mixes = _out(mixes, "mixes", lead + (mix,), torch.float32, dev)
-    with _on_device(dev):
-        _check(lib().hc_mixes(n, hc, d, float(norm_eps), _ptr(x), _ptr(w_mix), _ptr(mixes),
-                              _stream(dev, stream)), "hc_mixes")
+    _check(_call(dev, lib().hc_mixes, n, hc, d, float(norm_eps), _ptr(x), _ptr(w_mix),
+                 _ptr(mixes), _stream(dev, stream)), "hc_mixes")
     return mixes
 
 
@@ -183,10 +179,9 @@ def hc_split_sinkhorn(mixes, hc_scale, hc_base, hc_mult: int = 4, sinkhorn_iters
     pre = _out(pre, "pre", lead + (hc,), torch.float32, dev)
     post = _out(post, "post", lead + (hc,), torch.float32, dev)
     comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
-    with _on_device(dev):
-        _check(lib().hc_split_sinkhorn(n, hc, int(sinkhorn_iters), float(eps), _ptr(mixes),
-                                       _ptr(hc_scale), _ptr(hc_base), _ptr(pre), _ptr(post),
-                                       _ptr(comb), _stream(dev, stream)), "hc_split_sinkhorn")
+    _check(_call(dev, lib().hc_split_sinkhorn, n, hc, int(sinkhorn_iters), float(eps),
+                 _ptr(mixes), _ptr(hc_scale), _ptr(hc_base), _ptr(pre), _ptr(post), _ptr(comb),
+                 _stream(dev, stream)), "hc_split_sinkhorn")
     return pre, post, comb
 
 
@@ -199,9 +194,8 @@ def hc_pre(x, pre, y=None, stream=None):
     if pre.numel() != n * hc:
         raise ValueError("pre must hold n*hc values")
     y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
-    with _on_device(dev):
-        _check(lib().hc_pre(n, hc, d, _ptr(x), _ptr(pre), _ptr(y), _stream(dev, stream)),
-               "hc_pre")
+    _check(_call(dev, lib().hc_pre, n, hc, d, _ptr(x), _ptr(pre), _ptr(y), _stream(dev, stream)),
+           "hc_pre")
     return y
 
 
@@ -219,9 +213,8 @@ def hc_post(out, residual, post, comb, y=None, stream=None):
     if post.numel() != n * hc or comb.numel() != n * hc * hc:
         raise ValueError("post/comb sizes do not match residual")
     y = _out(y, "y", lead + (hc, d), torch.bfloat16, dev)
-    with _on_device(dev):
-        _check(lib().hc_post(n, hc, d, _ptr(out), _ptr(residual), _ptr(post), _ptr(comb), _ptr(y),
-                             _stream(dev, stream)), "hc_post")
+    _check(_call(dev, lib().hc_post, n, hc, d, _ptr(out), _ptr(residual), _ptr(post), _ptr(comb),
+                 _ptr(y), _stream(dev, stream)), "hc_post")
     return y
 
 
@@ -251,11 +244,10 @@ def hc_mixes_pre(x, w_mix, hc_scale, hc_base, sinkhorn_iters: int = 20, eps: flo
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
         wbytes = workspace.numel()
-    with _on_device(dev):
-        _check(lib().hc_mixes_pre(n, hc, d, int(sinkhorn_iters), float(eps), float(norm_eps),
-                                  _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
-                                  _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb), _ptr(y),
-                                  _ptr(workspace), wbytes, _stream(dev, stream)), "hc_mixes_pre")
+    _check(_call(dev, lib().hc_mixes_pre, n, hc, d, int(sinkhorn_iters), float(eps),
+                 float(norm_eps), _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
+                 _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb), _ptr(y), _ptr(workspace), wbytes,
+                 _stream(dev, stream)), "hc_mixes_pre")
     return y, pre, post, comb, mixes
 
 
@@ -289,12 +281,10 @@ def hc_mixes_pre_norm(x, w_mix, hc_scale, hc_base, rms_weight, sinkhorn_iters: i
     if workspace is not None:
         _need(workspace, "workspace", torch.uint8, dev)
         wbytes = workspace.numel()
-    with _on_device(dev):
-        _check(lib().hc_mixes_pre_norm(n, hc, d, int(sinkhorn_iters), float(eps), float(norm_eps),
-                                       _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
-                                       _ptr(rms_weight), float(rms_eps), _ptr(mixes), _ptr(pre),
-                                       _ptr(post), _ptr(comb), _ptr(y), _ptr(workspace), wbytes,
-                                       _stream(dev, stream)), "hc_mixes_pre_norm")
+    _check(_call(dev, lib().hc_mixes_pre_norm, n, hc, d, int(sinkhorn_iters), float(eps),
+                 float(norm_eps), _ptr(x), _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base),
+                 _ptr(rms_weight), float(rms_eps), _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb),
+                 _ptr(y), _ptr(workspace), wbytes, _stream(dev, stream)), "hc_mixes_pre_norm")
     return y, pre, post, comb, mixes
 
 
@@ -314,6 +304,5 @@ def hc_selftest_wait_timeout(limit_ns: int = 1000000, device=None, stream=None) 
     """Enqueues the library's bounded-wait self-test: a wait that can only
     time out, after which hc_device_error() reports bit 0."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
-    with _on_device(dev):
-        _check(lib().hc_selftest_wait_timeout(int(limit_ns), _stream(dev, stream)),
-               "hc_selftest_wait_timeout")
+    _check(_call(dev, lib().hc_selftest_wait_timeout, int(limit_ns), _stream(dev, stream)),
+           "hc_selftest_wait_timeout")
