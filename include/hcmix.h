@@ -4,9 +4,8 @@
  *
  * The operations are those of the "DeepSeek V4.1" model-atlas pages:
  *   hc_mixes           "Mix projection" page: formula for m and Block.hc_mixes
- *                      (model.py 948-966)
  *   hc_split_sinkhorn  "Reading weights" page: pre formula and the
- *                      hc_split_sinkhorn kernel and wrapper (kernel.py 406-474)
+ *                      hc_split_sinkhorn kernel and its wrapper
  *   hc_pre, hc_post    "Mix projection" page: Block.hc_pre, Block.hc_post
  *   hc_mixes_pre       the first three fused: what one sublayer needs before
  *                      it runs (Block docstring on the same page)

@@ -8,15 +8,15 @@
  * the seeded input generators.
  *
  * Sources (all on the "DeepSeek V4.1" model-atlas pages):
- *   - "Mix projection" page, the formula for m and the code of Block.hc_mixes
- *     (model.py 948-966): m = x^f W_mix^T / sqrt(mean((x^f)^2) + norm_eps),
+ *   - "Mix projection" page, the formula for m and the code of Block.hc_mixes:
+ *     m = x^f W_mix^T / sqrt(mean((x^f)^2) + norm_eps),
  *     one statistic per token over all hc*d features, x^f = x.flatten(2), so
  *     feature f = j*d + c for copy j and channel c.
- *   - "Reading weights" page, the pre formula and the hc_split_sinkhorn kernel
- *     (kernel.py 406-474): pre/post sigmoids, then a row softmax plus eps,
+ *   - "Reading weights" page, the pre formula and the hc_split_sinkhorn kernel:
+ *     pre/post sigmoids, then a row softmax plus eps,
  *     a column normalisation and iters-1 rounds of row-then-column
  *     normalisation, every later denominator being (sum + eps).
- *   - "Mix projection" page, Block.hc_pre and Block.hc_post (model.py 948-966).
+ *   - "Mix projection" page, the code of Block.hc_pre and Block.hc_post.
  *   - The RMSNorm the block applies to hc_pre's output (attn_norm / ffn_norm)
  *     is named but not shown on the pages: the standard form is taken (see
  *     orc_hc_rmsnorm).
