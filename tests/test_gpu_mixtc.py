@@ -120,3 +120,25 @@ def test_projection_only_dispatch_by_token_count(hc, path, n):
                                     np.random.default_rng(n).integers(0, n, 200)]))
     compare.check_mixes(np64(auto)[idx], oracle.hc_mixes(inputs.bf16_bits(x[idx]),
                                                          w.cpu().numpy()))
+
+
+def test_bench_projection_mode_agrees_across_kernels(hc):
+    # `bench.py --projection` times hc_mixes on the CUDA-core kernel, the
+    # streamed-W tensor-core kernel and the fused kernel's projection-only
+    # mode; on a 4,096-token case each is one launch and all agree with the
+    # CUDA-core result to the mixes tolerance
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--projection",
+                        "--tokens", "4096", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    proj = line["projection"]
+    assert set(proj) == {"ffma", "general", "fused"}
+    for name, rec in proj.items():
+        assert rec["launches_per_call"] == 1, name
+        assert rec["us_per_launch"] > 0
+        assert rec["max_rel_diff_vs_ffma"] <= 1e-4, (name, rec["max_rel_diff_vs_ffma"])
