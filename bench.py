@@ -53,6 +53,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
                     help="skip the 64-token decode latency line item")
+    ap.add_argument("--no-norm", action="store_true",
+                    help="skip the hc_mixes_pre_norm line item")
     ap.add_argument("--projection", action="store_true",
                     help="instead of the step: time the mix projection (hc_mixes) on its "
                          "CUDA-core (FFMA) kernel and on the tensor-core kernels, one JSON line")
@@ -247,6 +249,39 @@ def decode_latency(hc, dev, reps=20, replays=10):
             "us_per_step_eager": eager_us, "tokens_per_s_graph": n / graph_us * 1e6,
             "l2": "warm (inputs stay in L2 between steps)",
             "graph": "%d steps per captured graph, %d replays" % (reps, replays)}
+
+
+def norm_timing(hc, wl, x, p, iters, wsp, peak, dev, reps=20):
+    """hc_mixes_pre_norm (the collapse followed by the sublayer-input RMSNorm)
+    on the step's inputs, `reps` launches timed with CUDA events, against the
+    algorithmic bytes of hc_mixes_pre plus the RMSNorm weight."""
+    import torch
+    n, H, d = x.shape[0], x.shape[1], x.shape[2]
+    g = torch.Generator(device=dev).manual_seed(7)
+    rw = torch.rand(d, device=dev, generator=g) * 1.5 + 0.25
+    pre = torch.empty((n, H), device=dev)
+    post = torch.empty((n, H), device=dev)
+    comb = torch.empty((n, H, H), device=dev)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+
+    def call():
+        hc.hc_mixes_pre_norm(x, p["w"], p["hc_scale"], p["hc_base"], rw, iters, wl.eps,
+                             wl.norm_eps, pre=pre, post=post, comb=comb, y=y, workspace=wsp)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    launches0 = hc.hc_launch_count()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize(dev)
+    t = a.elapsed_time(b) / 1e3 / reps
+    nb = bytes_mixes_pre(n, H, d) + d * 4
+    return {"us_per_launch": 1e6 * t, "launches_per_call": (hc.hc_launch_count() - launches0) // reps,
+            "algorithmic_bytes": nb, "GBps": nb / t / 1e9, "frac": nb / t / 1e9 / peak,
+            "reps": reps}
 
 
 def e2e_pipelined(hc, args, wl, x, out, p, iters, ws, dev, chunks=8):
@@ -595,6 +630,10 @@ def run_ours(args, wl, ws, rank, local):
         "e2e": e2e,
         "gpu_launches": int(launches),
     }
+    if not args.no_norm:
+        line["norm"] = norm_timing(hc, wl, x, p, iters, wsp, peak, dev)
+        if hc.hc_device_error(clear=True):
+            raise RuntimeError("device error word set during the RMSNorm measurement")
     if not args.no_decode:
         line["decode"] = decode_latency(hc, dev)
         if hc.hc_device_error(clear=True):
