@@ -240,34 +240,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpProducer && lane == 0)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap))
                      : "memory");
-    // W slice -> bf16 hi/lo rows in the swizzled K-major layout.  Row nr < 24
-    // holds hi(W[nr]), row 24 + i holds lo(W[i]) = bf16(W - hi).
+    // W slice -> bf16 hi/lo rows in the swizzled K-major layout.  Row i < 24
+    // holds hi(W[i]), row 24 + i holds lo(W[i]) = bf16(W - hi).  Each 8-float
+    // piece of W is read once for both rows, with kPieces pieces in flight
+    // per thread (one piece at a time waited a full L2 round trip each).
     {
+        constexpr int kPieces = 8;
         const int nkc = 4 * ncc;
-        const int total = kNW * nkc * 8;
+        const int total = kMix * nkc * 8;  // (piece q, row i, chunk kc)
         const int64_t F = 4LL * p.d;
-        for (int idx = threadIdx.x; idx < total; idx += kThreads) {
-            const int q = idx & 7, rest = idx >> 3;
-            const int nr = rest % kNW, kc = rest / kNW;
-            const int i = nr % kMix;
-            const bool lo = nr >= kMix;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                p.w + (int64_t)i * F + chunk_feature(kc, rank, p) + q * 8);
-            const float4 a = __ldg(src), b2 = __ldg(src + 1);
-            float v[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
-            if (lo) {
+        for (int base = threadIdx.x; base < total; base += kPieces * kThreads) {
+            float4 a[kPieces], b2[kPieces];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    v[e] = v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+            for (int u = 0; u < kPieces; ++u) {
+                const int idx = base + u * kThreads;
+                if (idx < total) {
+                    const int q = idx & 7, rest = idx >> 3;
+                    const int i = rest % kMix, kc = rest / kMix;
+                    const float4 *src = reinterpret_cast<const float4 *>(
+                        p.w + (int64_t)i * F + chunk_feature(kc, rank, p) + q * 8);
+                    a[u] = __ldg(src);
+                    b2[u] = __ldg(src + 1);
+                }
             }
-            uint4 o;
-            o.x = pack_bf16x2(v[0], v[1]);
-            o.y = pack_bf16x2(v[2], v[3]);
-            o.z = pack_bf16x2(v[4], v[5]);
-            o.w = pack_bf16x2(v[6], v[7]);
-            uint8_t *dst = sm.w + (size_t)kc * kWChunkBytes + (nr >> 3) * 1024 + (nr & 7) * 128 +
-                           ((q ^ (nr & 7)) << 4);
-            *reinterpret_cast<uint4 *>(dst) = o;
+#pragma unroll
+            for (int u = 0; u < kPieces; ++u) {
+                const int idx = base + u * kThreads;
+                if (idx < total) {
+                    const int q = idx & 7, rest = idx >> 3;
+                    const int i = rest % kMix, kc = rest / kMix;
+                    float v[8] = {a[u].x, a[u].y, a[u].z, a[u].w,
+                                  b2[u].x, b2[u].y, b2[u].z, b2[u].w};
+                    float lo[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        lo[e] = v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+                    uint4 h, l;
+                    h.x = pack_bf16x2(v[0], v[1]);
+                    h.y = pack_bf16x2(v[2], v[3]);
+                    h.z = pack_bf16x2(v[4], v[5]);
+                    h.w = pack_bf16x2(v[6], v[7]);
+                    l.x = pack_bf16x2(lo[0], lo[1]);
+                    l.y = pack_bf16x2(lo[2], lo[3]);
+                    l.z = pack_bf16x2(lo[4], lo[5]);
+                    l.w = pack_bf16x2(lo[6], lo[7]);
+                    uint8_t *chunk = sm.w + (size_t)kc * kWChunkBytes;
+                    const int rl = kMix + i;
+                    *reinterpret_cast<uint4 *>(chunk + (i >> 3) * 1024 + (i & 7) * 128 +
+                                               ((q ^ (i & 7)) << 4)) = h;
+                    *reinterpret_cast<uint4 *>(chunk + (rl >> 3) * 1024 + (rl & 7) * 128 +
+                                               ((q ^ (rl & 7)) << 4)) = l;
+                }
+            }
         }
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
