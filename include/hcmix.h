@@ -126,10 +126,16 @@ hc_status hc_post(int64_t n, int hc, int64_t d, const uint16_t *out,
  *   mixes [n, mix_hc] float (out, may be NULL)
  *   pre, post [n, hc], comb [n, hc, hc] float (out)
  *   y [n, d] bf16 (out) -- the collapsed sublayer input
- *   workspace: device scratch of at least hc_workspace_bytes(n, hc, d)
- *   bytes, 256-byte aligned, not shared with another call in flight.  It is
- *   required when mixes is NULL (it may then hold the mix numbers between
- *   the kernels of the general path) and ignored otherwise (may be NULL).
+ *   workspace: device scratch, 256-byte aligned, not shared with another
+ *   call in flight.  hc_workspace_bytes(n, hc, d) is the size that gives
+ *   the fastest path.  When mixes is NULL the workspace is required and must
+ *   hold at least the mix numbers (n * mix_hc floats, rounded up to 256
+ *   bytes), which the general path keeps there between its kernels.  At
+ *   hc = 8 the rest of it (or all of it when mixes is given) also takes W
+ *   converted to the tensor core's bf16 hi/lo rows (4 * mix_hc * hc*d
+ *   bytes); a workspace without that room, or NULL when mixes is given, is
+ *   accepted and the projection then converts W inside its kernel (slower,
+ *   same results bit for bit).
  */
 hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps,
                        float norm_eps, const uint16_t *x, const float *w_mix,
@@ -157,9 +163,10 @@ hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
                             void *workspace, size_t workspace_bytes,
                             hc_stream_t stream);
 
-/* Scratch bytes hc_mixes_pre(_norm) may need for these sizes when mixes is NULL
- * (n * mix_hc floats, rounded up to 256 bytes; 0 for n == 0 or invalid
- * sizes).  Pure host function; the value depends only on its arguments. */
+/* Scratch bytes for hc_mixes_pre(_norm) at these sizes: n * mix_hc floats
+ * rounded up to 256 bytes, plus at hc = 8 the converted W (4 * mix_hc * hc*d
+ * bytes, rounded up to 256); 0 for n == 0 or invalid sizes.  Pure host
+ * function; the value depends only on its arguments. */
 size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
 
 /*

@@ -237,7 +237,9 @@ def hc_mixes_pre(x, w_mix, hc_scale, hc_base, sinkhorn_iters: int = 20, eps: flo
     comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
     y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
     wbytes = 0
-    if mixes is None:
+    if mixes is None or hc == 8:
+        # the mix numbers when not returned; at hc = 8 also W converted for
+        # the tensor-core projection (hcmix.h, hc_workspace_bytes)
         wbytes = hc_workspace_bytes(n, hc, d)
         if workspace is None and wbytes:
             workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
@@ -274,7 +276,7 @@ def hc_mixes_pre_norm(x, w_mix, hc_scale, hc_base, rms_weight, sinkhorn_iters: i
     comb = _out(comb, "comb", lead + (hc, hc), torch.float32, dev)
     y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
     wbytes = 0
-    if mixes is None:
+    if mixes is None or hc == 8:
         wbytes = hc_workspace_bytes(n, hc, d)
         if workspace is None and wbytes:
             workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)

@@ -52,9 +52,10 @@ ForcedPath forced_path() {
 
 // The projection of the general path: tensor cores when they take the shape.
 cudaError_t launch_projection(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
-                              const float *w, float *mixes, const DeviceInfo &di,
-                              cudaStream_t s) {
-    if (mixtc_supported(hc, d, di)) return launch_mixtc(n, hc, d, norm_eps, x, w, mixes, di, s);
+                              const float *w, float *mixes, uint16_t *wconv,
+                              const DeviceInfo &di, cudaStream_t s) {
+    if (mixtc_supported(hc, d, di))
+        return launch_mixtc(n, hc, d, norm_eps, x, w, mixes, wconv, di, s);
     return launch_mixes(n, hc, d, norm_eps, x, w, mixes, di, s);
 }
 
@@ -159,10 +160,15 @@ int hc_abi_version(void) { return HCMIX_ABI_VERSION; }
 
 uint64_t hc_launch_count(void) { return hc::g_launches.load(std::memory_order_relaxed); }
 
+namespace {
+uint64_t round256(uint64_t b) { return (b + 255u) / 256u * 256u; }
+// bytes of the workspace's first part: the mix numbers when mixes is NULL
+uint64_t mix_part_bytes(int64_t n, int hc) { return round256((uint64_t)n * ((2 + hc) * hc) * 4u); }
+}  // namespace
+
 size_t hc_workspace_bytes(int64_t n, int hc, int64_t d) {
     if (check_shape(n, hc, d) != HC_OK || n == 0) return 0;
-    const uint64_t b = (uint64_t)n * (uint64_t)((2 + hc) * hc) * 4u;
-    return (size_t)((b + 255u) / 256u * 256u);
+    return (size_t)(mix_part_bytes(n, hc) + round256(hc::mixtc_wconv_bytes(hc, d)));
 }
 
 // Token count from which hc_mixes takes the streamed-W tensor-core kernel
@@ -202,7 +208,7 @@ hc_status hc_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t 
                                           w_mix, nullptr, nullptr, mixes, nullptr, nullptr,
                                           nullptr, nullptr, di, s));
     }
-    return from_cuda(hc::launch_projection(n, hc, d, norm_eps, x, w_mix, mixes, di, s));
+    return from_cuda(hc::launch_projection(n, hc, d, norm_eps, x, w_mix, mixes, nullptr, di, s));
 }
 
 hc_status hc_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,
@@ -287,7 +293,7 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
     // the mix numbers in it between its stages).
     float *m = mixes;
     if (m == nullptr) {
-        if (workspace == nullptr || workspace_bytes < hc_workspace_bytes(n, hc, d))
+        if (workspace == nullptr || workspace_bytes < mix_part_bytes(n, hc))
             return HC_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HC_ERR_MISALIGNED;
         m = static_cast<float *>(workspace);
@@ -318,8 +324,26 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
             e = hc::launch_rmsnorm(n, d, y, rms_w, rms_eps, di, s);
         return from_cuda(e);
     }
-    // General path: three kernels, the mix numbers passing through m.
-    cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, m, di, s);
+    // General path: three kernels, the mix numbers passing through m.  A
+    // workspace with room past the mix numbers (hc_workspace_bytes) also
+    // takes the converted W; one that is smaller, misaligned or overlapping
+    // is simply not used for it.
+    uint16_t *wconv = nullptr;
+    const uint64_t wcb = hc::mixtc_wconv_bytes(hc, d);
+    if (wcb != 0 && workspace != nullptr &&
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0) {
+        const uint64_t off = mixes == nullptr ? mix_part_bytes(n, hc) : 0;
+        if (workspace_bytes >= off + wcb) {
+            uint16_t *cand = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(workspace) + off);
+            if (disjoint({rng(cand, wcb)},
+                         {rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
+                          rng(comb, n * (uint64_t)hc * hc * 4ull), rng(y, (uint64_t)n * d * 2),
+                          rng(x, n * F * 2), rng(w_mix, mix * F * 4), rng(hc_scale, 12),
+                          rng(hc_base, mix * 4), rrms, rng(m, n * mix * 4)}))
+                wconv = cand;
+        }
+    }
+    cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, m, wconv, di, s);
     if (e == cudaSuccess)
         e = hc::launch_split_sinkhorn(n, hc, iters, eps, m, hc_scale, hc_base, pre, post, comb,
                                       di, s);

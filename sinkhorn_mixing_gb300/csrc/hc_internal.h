@@ -42,16 +42,20 @@ cudaError_t launch_mixes(int64_t n, int hc, int64_t d, float norm_eps, const uin
                          const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s);
 
 // The general path's projection: launch_mixtc when it takes the shape, else
-// launch_mixes.
+// launch_mixes.  wconv (nullable, 16-byte aligned, mixtc_wconv_bytes(hc, d)
+// bytes) is device scratch for W converted to the tensor core's hi/lo rows.
 cudaError_t launch_projection(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
-                              const float *w, float *mixes, const DeviceInfo &di,
-                              cudaStream_t s);
+                              const float *w, float *mixes, uint16_t *wconv,
+                              const DeviceInfo &di, cudaStream_t s);
 
 // Tensor-core projection with W streamed (hc_mixtc.cu): hc in {4, 8} and
-// hc*d a multiple of 64.
+// hc*d a multiple of 64.  With wconv (hc = 8 only) W is converted once into
+// it and loaded from there; without, the kernel converts it stage by stage.
 bool mixtc_supported(int hc, int64_t d, const DeviceInfo &di);
+size_t mixtc_wconv_bytes(int hc, int64_t d);  // 0 where no conversion pass is used
 cudaError_t launch_mixtc(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
-                         const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s);
+                         const float *w, float *mixes, uint16_t *wconv, const DeviceInfo &di,
+                         cudaStream_t s);
 
 cudaError_t launch_split_sinkhorn(int64_t n, int hc, int iters, float eps, const float *mixes,
                                   const float *scale, const float *base, float *pre,

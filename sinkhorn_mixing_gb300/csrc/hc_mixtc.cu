@@ -12,7 +12,10 @@
 //     unit is two tiles sharing every W stage.
 //   * 4 convert warps split the W sub-tile into bf16 hi rows (bf16(W)) and lo
 //     rows (bf16(W - hi)) in the swizzled K-major layout the tensor core
-//     reads, so no converted copy of W is kept in memory.
+//     reads.  At hc = 8 that conversion is a fifth of the kernel's shared-
+//     memory traffic, so when the caller provides room, k_convert_w writes
+//     the hi/lo rows to global memory once per call and the kernel (PRE)
+//     loads them by TMA, already swizzled, with a deeper ring.
 //   * Per stage and tile, 4 tcgen05.mma (M = 128 tokens, N = 2*mix rows of hi
 //     and lo, K = 16) accumulate x.(W_hi + W_lo) in TMEM (binary32).  bf16 x is exact
 //     and hi + lo carries ~16 mantissa bits of W.  The tensor core's own
@@ -54,13 +57,13 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpSq0 = 2;
 constexpr int kWarpEpi0 = 8;
 
-template <int HC>
+template <int HC, bool PRE = false>
 struct Cfg {
     static constexpr int kMix = (2 + HC) * HC;      // 24 or 80
     static constexpr int kNW = 2 * kMix;            // B rows: hi then lo
     static constexpr int kTPU = HC == 8 ? 2 : 1;    // tiles per unit
     static constexpr int kAccBufs = kTPU == 1 ? 2 : 1;
-    static constexpr int kStages = HC == 8 ? 3 : 6;
+    static constexpr int kStages = HC == 8 ? (PRE ? 4 : 3) : 6;
     static constexpr int kWfBytes = kMix * kK * 4;  // fp32 W sub-tile
     static constexpr int kWbBytes = kNW * kK * 2;   // bf16 hi/lo sub-tile
     static constexpr int kXStage = kTPU * kXBytes;  // x sub-tiles of a stage
@@ -92,16 +95,17 @@ struct MixParams {
     unsigned int *err;
 };
 
-template <int HC>
+template <int HC, bool PRE>
 __host__ __device__ constexpr size_t ring_bytes() {
-    return (size_t)Cfg<HC>::kStages * (Cfg<HC>::kXStage + Cfg<HC>::kWbBytes + Cfg<HC>::kWfBytes);
+    using C = Cfg<HC, PRE>;
+    return (size_t)C::kStages * (C::kXStage + C::kWbBytes + (PRE ? 0 : C::kWfBytes));
 }
 
 // barrier indices
-template <int HC>
+template <int HC, bool PRE>
 struct Bars {
-    static constexpr int S = Cfg<HC>::kStages;
-    static constexpr int A = Cfg<HC>::kAccBufs;
+    static constexpr int S = Cfg<HC, PRE>::kStages;
+    static constexpr int A = Cfg<HC, PRE>::kAccBufs;
     static constexpr int full(int s) { return s; }
     static constexpr int conv(int s) { return S + s; }
     static constexpr int empty(int s) { return 2 * S + s; }
@@ -113,18 +117,53 @@ struct Bars {
     static constexpr int count = drain + 1;
 };
 
-template <int HC>
+template <int HC, bool PRE>
 __host__ __device__ constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + ring_bytes<HC>() + 2 * Cfg<HC>::kTPU * kTok * 4 +
-           Bars<HC>::count * 8 + 16;
+    return 1024 /* alignment slack */ + ring_bytes<HC, PRE>() + 2 * Cfg<HC, PRE>::kTPU * kTok * 4 +
+           Bars<HC, PRE>::count * 8 + 16;
 }
 
+// W fp32 [kMix][F] -> the B rows of every 64-feature stage, bf16, unswizzled:
+// wc[kc][r][64] with r < kMix the hi rows bf16(W) and r = kMix + i the lo rows
+// bf16(W - hi) -- the same numbers the convert warps write into shared memory.
 template <int HC>
-__global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
+__global__ void __launch_bounds__(256) k_convert_w(int F, const float *__restrict__ w,
+                                                   uint4 *__restrict__ wc) {
+    constexpr int kMix = Cfg<HC>::kMix;
+    const int64_t total = (int64_t)(F / kK) * kMix * 8;  // (stage, row, 8-feature piece)
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int q = (int)(e & 7);
+        const int64_t rest = e >> 3;
+        const int i = (int)(rest % kMix);
+        const int64_t kc = rest / kMix;
+        const float4 *src = reinterpret_cast<const float4 *>(w + (int64_t)i * F + kc * kK + q * 8);
+        const float4 a = __ldg(src), b2 = __ldg(src + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b2.x, b2.y, b2.z, b2.w};
+        float lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lo[u] = v[u] - __bfloat162float(__float2bfloat16_rn(v[u]));
+        uint4 hv, lv;
+        hv.x = pack_bf16x2(v[0], v[1]);
+        hv.y = pack_bf16x2(v[2], v[3]);
+        hv.z = pack_bf16x2(v[4], v[5]);
+        hv.w = pack_bf16x2(v[6], v[7]);
+        lv.x = pack_bf16x2(lo[0], lo[1]);
+        lv.y = pack_bf16x2(lo[2], lo[3]);
+        lv.z = pack_bf16x2(lo[4], lo[5]);
+        lv.w = pack_bf16x2(lo[6], lo[7]);
+        uint4 *st = wc + kc * (2 * kMix) * 8;  // stage kc: 2*kMix rows of 8 pieces
+        st[i * 8 + q] = hv;
+        st[(kMix + i) * 8 + q] = lv;
+    }
+}
+
+template <int HC, bool PRE>
+__global__ void __launch_bounds__(Cfg<HC, PRE>::kThreads, 1)
     k_mixtc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
             const MixParams p) {
-    using C = Cfg<HC>;
-    using B = Bars<HC>;
+    using C = Cfg<HC, PRE>;
+    using B = Bars<HC, PRE>;
     constexpr int S = C::kStages;
     constexpr int TPU = C::kTPU;
     constexpr int AB = C::kAccBufs;
@@ -133,8 +172,8 @@ __global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *xr = base;                               // [S][TPU][128 x 64] bf16, swizzled
     uint8_t *wb = xr + (size_t)S * C::kXStage;        // [S][kNW x 64] bf16, swizzled
-    float *wf = reinterpret_cast<float *>(wb + (size_t)S * C::kWbBytes);  // [S][kMix][64]
-    float *sq = wf + (size_t)S * C::kMix * kK;        // [2][TPU][128]
+    float *wf = reinterpret_cast<float *>(wb + (size_t)S * C::kWbBytes);  // [S][kMix][64], !PRE
+    float *sq = wf + (PRE ? 0 : (size_t)S * C::kMix * kK);  // [2][TPU][128]
     uint64_t *bars = reinterpret_cast<uint64_t *>(sq + 2 * TPU * kTok);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B::count);
     int *abort_word = reinterpret_cast<int *>(tmem_slot + 1);
@@ -190,14 +229,19 @@ __global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(B::full(slot)), (uint32_t)(C::kXStage + C::kWfBytes));
+                    mbar_expect_tx(bar(B::full(slot)),
+                                   (uint32_t)(C::kXStage + (PRE ? C::kWbBytes : C::kWfBytes)));
                     // a unit's second tile past the last token reads zeros
 #pragma unroll
                     for (int v = 0; v < TPU; ++v)
                         tma_load_2d(su32(xr + (size_t)slot * C::kXStage + v * kXBytes), &tm_x,
                                     kc * kK, (unit * TPU + v) * kTok, bar(B::full(slot)));
-                    tma_load_2d(su32(wf + (size_t)slot * C::kMix * kK), &tm_w, kc * kK, 0,
-                                bar(B::full(slot)));
+                    if (PRE)  // the stage's hi/lo rows, swizzled on the way in
+                        tma_load_2d(su32(wb + (size_t)slot * C::kWbBytes), &tm_w, 0, kc * C::kNW,
+                                    bar(B::full(slot)));
+                    else
+                        tma_load_2d(su32(wf + (size_t)slot * C::kMix * kK), &tm_w, kc * kK, 0,
+                                    bar(B::full(slot)));
                     last_use[slot] = (int)use;
                 }
             }
@@ -221,7 +265,7 @@ __global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
                         const int slot = (int)(q % S);
                         const uint32_t par = (q / S) & 1;
                         if (!wait_bar<false>(bar(B::full(slot)), par, abort, p.err) ||
-                            !wait_bar<false>(bar(B::conv(slot)), par, abort, p.err)) {
+                            (!PRE && !wait_bar<false>(bar(B::conv(slot)), par, abort, p.err))) {
                             ok = false;
                             break;
                         }
@@ -246,7 +290,7 @@ __global__ void __launch_bounds__(Cfg<HC>::kThreads, 1)
             mma_commit(bar(B::drain));
             wait_bar<false>(bar(B::drain), 0, abort, p.err);
         }
-    } else if (C::is_convert(warp)) {
+    } else if (C::is_convert(warp) && !PRE) {
         // W sub-tile (fp32 rows of 64) -> bf16 hi rows 0..kMix-1 and lo rows
         // kMix..2kMix-1, 8 features per 16-byte chunk, swizzled K-major.
         const int ci = C::convert_index(warp) * 32 + lane;
@@ -410,10 +454,10 @@ struct DevState {
 std::mutex g_mmu;
 DevState g_mix[64];
 
-template <int HC>
+template <int HC, bool PRE>
 bool set_attrs() {
-    return cudaFuncSetAttribute(k_mixtc<HC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem_bytes<HC>()) == cudaSuccess;
+    return cudaFuncSetAttribute(k_mixtc<HC, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes<HC, PRE>()) == cudaSuccess;
 }
 
 const DevState &mix_state(const DeviceInfo &di) {
@@ -425,7 +469,7 @@ const DevState &mix_state(const DeviceInfo &di) {
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
     if (tensor_map_encoder() == nullptr) return st;
-    if (!set_attrs<4>() || !set_attrs<8>()) {
+    if (!set_attrs<4, false>() || !set_attrs<8, false>() || !set_attrs<8, true>()) {
         cudaGetLastError();
         return st;
     }
@@ -435,9 +479,11 @@ const DevState &mix_state(const DeviceInfo &di) {
 
 template <int HC>
 cudaError_t launch(int64_t n, int64_t d, float norm_eps, const uint16_t *x, const float *w,
-                   float *mixes, const DeviceInfo &di, cudaStream_t s) {
+                   float *mixes, uint16_t *wconv, const DeviceInfo &di, cudaStream_t s) {
     constexpr int MIX = (2 + HC) * HC;
+    constexpr bool kCanPre = HC == 8;  // where the conversion is worth a pass of its own
     const int64_t F = (int64_t)HC * d;
+    const bool pre = kCanPre && wconv != nullptr;
     CUtensorMap tm_x, tm_w;
     {
         // x as [n rows][F] bf16; one box = 64 features of 128 tokens, swizzled
@@ -452,7 +498,19 @@ cudaError_t launch(int64_t n, int64_t d, float norm_eps, const uint16_t *x, cons
                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    {
+    if (pre) {
+        // converted W as [(F/64) * 2 mix rows][64] bf16; one box = one stage's
+        // hi and lo rows, 128-byte swizzled like x
+        const cuuint64_t gdim[2] = {(cuuint64_t)kK, (cuuint64_t)(F / kK) * 2 * MIX};
+        const cuuint64_t gstride[1] = {(cuuint64_t)kK * 2};
+        const cuuint32_t box[2] = {kK, (cuuint32_t)(2 * MIX)};
+        const cuuint32_t es[2] = {1, 1};
+        if (tensor_map_encoder()(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wconv, gdim, gstride,
+                                 box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
         // W as [mix rows][F] fp32; one box = 64 features of every row
         const cuuint64_t gdim[2] = {(cuuint64_t)F, (cuuint64_t)MIX};
         const cuuint64_t gstride[1] = {(cuuint64_t)F * 4};
@@ -475,7 +533,20 @@ cudaError_t launch(int64_t n, int64_t d, float norm_eps, const uint16_t *x, cons
     p.mixes = mixes;
     p.err = di.err_word;
     const int grid = p.num_units < di.sms ? p.num_units : di.sms;
-    k_mixtc<HC><<<grid, Cfg<HC>::kThreads, smem_bytes<HC>(), s>>>(tm_x, tm_w, p);
+    if (pre) {
+        if constexpr (kCanPre) {
+            const int64_t items = (F / kK) * MIX * 8;
+            const int64_t cgrid = (items + 255) / 256 < (int64_t)di.sms * 8
+                                      ? (items + 255) / 256 : (int64_t)di.sms * 8;
+            k_convert_w<HC><<<(unsigned)cgrid, 256, 0, s>>>((int)F, w,
+                                                           reinterpret_cast<uint4 *>(wconv));
+            k_mixtc<HC, true><<<grid, Cfg<HC, true>::kThreads, smem_bytes<HC, true>(), s>>>(
+                tm_x, tm_w, p);
+            return launched(2);
+        }
+    }
+    k_mixtc<HC, false><<<grid, Cfg<HC, false>::kThreads, smem_bytes<HC, false>(), s>>>(tm_x,
+                                                                                       tm_w, p);
     return launched();
 }
 
@@ -488,11 +559,16 @@ bool mixtc_supported(int hc, int64_t d, const DeviceInfo &di) {
     return mix_state(di).ok;
 }
 
+size_t mixtc_wconv_bytes(int hc, int64_t d) {
+    return hc == 8 ? (size_t)4 * (size_t)((2 + hc) * hc) * (size_t)(hc * d) : 0;
+}
+
 cudaError_t launch_mixtc(int64_t n, int hc, int64_t d, float norm_eps, const uint16_t *x,
-                         const float *w, float *mixes, const DeviceInfo &di, cudaStream_t s) {
+                         const float *w, float *mixes, uint16_t *wconv, const DeviceInfo &di,
+                         cudaStream_t s) {
     if (!mix_state(di).ok || n < 1 || n >= ((int64_t)1 << 31)) return cudaErrorNotSupported;
-    return hc == 4 ? launch<4>(n, d, norm_eps, x, w, mixes, di, s)
-                   : launch<8>(n, d, norm_eps, x, w, mixes, di, s);
+    return hc == 4 ? launch<4>(n, d, norm_eps, x, w, mixes, nullptr, di, s)
+                   : launch<8>(n, d, norm_eps, x, w, mixes, wconv, di, s);
 }
 
 }  // namespace hc

@@ -128,7 +128,14 @@ def test_workspace_rules(L):
     assert need == 512  # 4 tokens x 24 floats = 384 bytes, rounded up to 256
     assert L.hc_workspace_bytes(0, 4, 64) == 0
     assert L.hc_workspace_bytes(4, 3, 64) == 0
-    assert L.hc_workspace_bytes(65536, 8, 5120) == 65536 * 80 * 4
+    # at hc = 8 it also holds W converted to the tensor core's hi/lo rows
+    # (2 * 80 rows x hc*d bf16), past the mix numbers
+    assert L.hc_workspace_bytes(65536, 8, 5120) == 65536 * 80 * 4 + 4 * 80 * 8 * 5120
+    assert L.hc_workspace_bytes(4, 8, 64) == 1280 + 4 * 80 * 512
+    # a workspace for the mix numbers alone is still accepted (W is then
+    # converted inside the projection kernel)
+    assert mixes_pre_call(L, hc=8, ws=fake(9), wsb=1280) in (OK, CUDA)
+    assert mixes_pre_call(L, hc=8, ws=fake(9), wsb=1279) == INVALID
     # no mixes and no workspace -> rejected before any CUDA call
     assert mixes_pre_call(L) == INVALID
     assert mixes_pre_call(L, ws=fake(9), wsb=need - 1) == INVALID

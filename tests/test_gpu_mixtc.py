@@ -92,7 +92,8 @@ def test_hc8_mixes_pre_through_tensor_projection(hc, path):
     before = hc.hc_launch_count()
     y, pre, post, comb, m = hc.hc_mixes_pre(x, w, sc, base, 20, want_mixes=True)
     torch.cuda.synchronize()
-    assert hc.hc_launch_count() - before == 3
+    # W conversion, projection, split/Sinkhorn, collapse
+    assert hc.hc_launch_count() - before == 4
     xb = inputs.bf16_bits(x)
     compare.check_mixes(np64(m), oracle.hc_mixes(xb, w.cpu().numpy()))
     o_pre, o_post, o_comb = oracle.hc_split_sinkhorn(np64(m), sc.cpu().numpy(),
@@ -142,3 +143,36 @@ def test_bench_projection_mode_agrees_across_kernels(hc):
         assert rec["launches_per_call"] == 1, name
         assert rec["us_per_launch"] > 0
         assert rec["max_rel_diff_vs_ffma"] <= 1e-4, (name, rec["max_rel_diff_vs_ffma"])
+
+
+
+@pytest.mark.parametrize("n,d", [(300, 5120), (129, 1024), (5, 64)])
+def test_hc8_projection_from_converted_w_is_bit_identical(hc, path, n, d):
+    # with room in the workspace W is converted once into it and the kernel
+    # loads it from there; without, the kernel converts each stage itself:
+    # the tensor core sees the same numbers in the same order
+    path(None)
+    H = 8
+    x, w = case(n, H, d, 23 + n)
+    g = torch.Generator(device="cuda").manual_seed(3)
+    sc = torch.rand(3, device="cuda", generator=g) + 0.5
+    base = torch.randn(80, device="cuda", generator=g)
+    need = hc.hc_workspace_bytes(n, H, d)
+    small = (n * 80 * 4 + 255) // 256 * 256
+    assert need > small
+    outs = []
+    for wsb in (need, small):
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        before = hc.hc_launch_count()
+        r = hc.hc_mixes_pre(x, w, sc, base, workspace=ws)
+        m = torch.empty((n, 80), device="cuda")
+        hc.hc_mixes_pre(x, w, sc, base, mixes=m, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((r, m, hc.hc_launch_count() - before))
+    (r1, m1, l1), (r2, m2, l2) = outs
+    assert l1 == 2 * 4 and l2 == 2 * 3  # converted W: 4 launches per call, else 3
+    assert torch.equal(m1.view(torch.int32), m2.view(torch.int32))
+    for a, b in zip(r1[:4], r2[:4]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+    compare.check_mixes(np64(m1), oracle.hc_mixes(inputs.bf16_bits(x), w.cpu().numpy()))
