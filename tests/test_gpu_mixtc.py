@@ -146,7 +146,7 @@ def test_bench_projection_mode_agrees_across_kernels(hc):
 
 
 
-@pytest.mark.parametrize("n,d", [(300, 5120), (129, 1024), (5, 64)])
+@pytest.mark.parametrize("n,d", [(300, 5120), (129, 1024), (5, 64), (3, 8)])
 def test_hc8_projection_from_converted_w_is_bit_identical(hc, path, n, d):
     # with room in the workspace W is converted once into it and the kernel
     # loads it from there; without, the kernel converts each stage itself:
