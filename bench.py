@@ -55,6 +55,8 @@ def parse(argv=None):
                     help="skip the 64-token decode latency line item")
     ap.add_argument("--no-norm", action="store_true",
                     help="skip the hc_mixes_pre_norm line item")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the prefill, prefill-pair and stress line items")
     ap.add_argument("--projection", action="store_true",
                     help="instead of the step: time the mix projection (hc_mixes) on its "
                          "CUDA-core (FFMA) kernel and on the tensor-core kernels, one JSON line")
@@ -369,6 +371,146 @@ def e2e_pipelined(hc, args, wl, x, out, p, iters, ws, dev, chunks=8):
                         % len(bounds)}
 
 
+def _flush_buffer(in_bytes, dev):
+    import torch
+    if in_bytes >= 2 * L2_BYTES:
+        return None
+    return torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+
+
+def workload_timing(hc, name, peak, dev, steps=20):
+    """One step (hc_mixes_pre + hc_post) of another workload, `steps` steps
+    timed per kernel with CUDA events on the launching stream, L2 flushed
+    between steps when the inputs are smaller than twice the L2."""
+    import torch
+    from sinkhorn_mixing_gb300 import inputs
+    wl = inputs.WORKLOADS[name]
+    n, H, d = wl.n, wl.hc, wl.d
+    iters = 20 if 20 in wl.iters else wl.iters[0]
+    s = inputs.make_streams(wl, device=dev)
+    p = inputs.make_params(wl, device=dev)
+    x, out = s["x"], s["out"]
+    pre = torch.empty((n, H), device=dev)
+    post = torch.empty((n, H), device=dev)
+    comb = torch.empty((n, H, H), device=dev)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+    ys = torch.empty((n, H, d), dtype=torch.bfloat16, device=dev)
+    wsp = torch.empty(max(256, hc.hc_workspace_bytes(n, H, d)), dtype=torch.uint8, device=dev)
+    flush = _flush_buffer(x.numel() * 2 + out.numel() * 2, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def k1():
+        hc.hc_mixes_pre(x, p["w"], p["hc_scale"], p["hc_base"], iters, wl.eps, wl.norm_eps,
+                        pre=pre, post=post, comb=comb, y=y, workspace=wsp)
+
+    def k2():
+        hc.hc_post(out, x, post, comb, y=ys)
+
+    for _ in range(3):
+        if flush is not None:
+            flush.zero_()
+        k1()
+        k2()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ev[i][0].record(stream)
+        k1()
+        ev[i][1].record(stream)
+        k2()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    a1 = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3 / steps
+    a2 = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3 / steps
+    b1, b2 = bytes_mixes_pre(n, H, d), bytes_post(n, H, d)
+    if hc.hc_device_error(clear=True):
+        raise RuntimeError("device error word set during the %s measurement" % name)
+    return {"workload": DESCR[name], "tokens": n, "iters": iters,
+            "tokens_per_s": n / (a1 + a2), "ms_per_step": 1e3 * (a1 + a2),
+            "GBps": (b1 + b2) / (a1 + a2) / 1e9,
+            "hc_mixes_pre": {"us_per_launch": 1e6 * a1, "algorithmic_bytes": b1,
+                             "GBps": b1 / a1 / 1e9, "frac": b1 / a1 / 1e9 / peak},
+            "hc_post": {"us_per_launch": 1e6 * a2, "algorithmic_bytes": b2,
+                        "GBps": b2 / a2 / 1e9, "frac": b2 / a2 / 1e9 / peak},
+            "step_frac_of_hbm_roofline": (b1 + b2) / (a1 + a2) / 1e9 / peak,
+            "steps": steps,
+            "l2": "flushed between steps" if flush is not None else "inputs larger than L2"}
+
+
+def pair_timing(hc, peak, dev, steps=20):
+    """The prefill workload as one block: the attention sublayer and the FFN
+    sublayer, each with its own parameter set (W_mix, hc_base, hc_scale) and
+    its own synthetic sublayer output, chained through the stream:
+      y_a = mixes_pre(x; A);  x1 = post(out_a, x; A)
+      y_f = mixes_pre(x1; F); x2 = post(out_f, x1; F)
+    Every coefficient set is used around its own sublayer.  L2 flushed before
+    each step; the four launches timed with CUDA events."""
+    import torch
+    from sinkhorn_mixing_gb300 import inputs
+    wl = inputs.WORKLOADS["prefill"]
+    n, H, d = wl.n, wl.hc, wl.d
+    s = inputs.make_streams(wl, device=dev)
+    s2 = inputs.make_streams(wl, device=dev, seed_offset=1)
+    pa = inputs.make_params(wl, 0, device=dev)
+    pf = inputs.make_params(wl, 1, device=dev)
+    x, out_a, out_f = s["x"], s["out"], s2["out"]
+    x1 = torch.empty_like(x)
+    x2 = torch.empty_like(x)
+
+    def coefs():
+        return (torch.empty((n, H), device=dev), torch.empty((n, H), device=dev),
+                torch.empty((n, H, H), device=dev),
+                torch.empty((n, d), dtype=torch.bfloat16, device=dev))
+    ca, cf = coefs(), coefs()
+    wsp = torch.empty(max(256, hc.hc_workspace_bytes(n, H, d)), dtype=torch.uint8, device=dev)
+    flush = _flush_buffer(3 * x.numel() * 2, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def sub(xin, xout, outv, p, c):
+        pre, post, comb, y = c
+        hc.hc_mixes_pre(xin, p["w"], p["hc_scale"], p["hc_base"], 20, wl.eps, wl.norm_eps,
+                        pre=pre, post=post, comb=comb, y=y, workspace=wsp)
+        mid.append(torch.cuda.Event(enable_timing=True))
+        mid[-1].record(stream)
+        hc.hc_post(outv, xin, post, comb, y=xout)
+
+    for _ in range(3):
+        mid = []
+        if flush is not None:
+            flush.zero_()
+        sub(x, x1, out_a, pa, ca)
+        sub(x1, x2, out_f, pf, cf)
+    torch.cuda.synchronize(dev)
+    t_mp = t_post = 0.0
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        mid = []
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        sub(x, x1, out_a, pa, ca)
+        m1.record(stream)
+        sub(x1, x2, out_f, pf, cf)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_mp += (e0.elapsed_time(mid[0]) + m1.elapsed_time(mid[1])) / 1e3
+        t_post += (mid[0].elapsed_time(m1) + mid[1].elapsed_time(e1)) / 1e3
+    tp = (t_mp + t_post) / steps
+    b = 2 * (bytes_mixes_pre(n, H, d) + bytes_post(n, H, d))
+    if hc.hc_device_error(clear=True):
+        raise RuntimeError("device error word set during the pair measurement")
+    return {"workload": DESCR["prefill"] + "; attention + FFN sublayers, two parameter sets",
+            "tokens": n, "us_per_pair": 1e6 * tp, "tokens_per_s": n / tp,
+            "sublayer_tokens_per_s": 2 * n / tp, "GBps": b / tp / 1e9,
+            "frac_of_hbm_roofline": b / tp / 1e9 / peak,
+            "hc_mixes_pre_us": 1e6 * t_mp / steps / 2, "hc_post_us": 1e6 * t_post / steps / 2,
+            "steps": steps, "l2": "flushed before each pair" if flush is not None
+            else "inputs larger than L2"}
+
+
 def cpu_baseline(wl, seconds):
     """The float64 oracle, as it stands, on a bounded sample of the workload's
     tokens (same recipe, drawn on the host), timed on this host's cores."""
@@ -617,7 +759,11 @@ def run_ours(args, wl, ws, rank, local):
                    "parallelism": "replicas" if ws == 1 else "dp%d (token shards)" % ws},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": (tr["dram_bytes_per_launch"] if tr else None)},
+                     "traffic": (tr["dram_bytes_per_launch"] if tr else None),
+                     "traffic_note": (("scaled in tokens from an ncu capture of %d tokens; "
+                                       "a lower bound: part of the last writes were still "
+                                       "in L2 when the capture ended" % tr["captured_tokens"])
+                                      if tr else None)},
         "kernels": {
             "hc_mixes_pre": {"us_per_launch": 1e6 * a1, "algorithmic_bytes": b1,
                              "GBps": b1 / a1 / 1e9, "frac": b1 / a1 / 1e9 / peak},
@@ -634,6 +780,10 @@ def run_ours(args, wl, ws, rank, local):
         line["norm"] = norm_timing(hc, wl, x, p, iters, wsp, peak, dev)
         if hc.hc_device_error(clear=True):
             raise RuntimeError("device error word set during the RMSNorm measurement")
+    if not args.no_configs and n == wl.n and args.workload == "large":
+        line["prefill"] = workload_timing(hc, "prefill", peak, dev)
+        line["prefill_pair"] = pair_timing(hc, peak, dev)
+        line["stress"] = workload_timing(hc, "stress", peak, dev)
     if not args.no_decode:
         line["decode"] = decode_latency(hc, dev)
         if hc.hc_device_error(clear=True):

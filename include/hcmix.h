@@ -126,16 +126,21 @@ hc_status hc_post(int64_t n, int hc, int64_t d, const uint16_t *out,
  *   mixes [n, mix_hc] float (out, may be NULL)
  *   pre, post [n, hc], comb [n, hc, hc] float (out)
  *   y [n, d] bf16 (out) -- the collapsed sublayer input
- *   workspace: device scratch, 256-byte aligned, not shared with another
- *   call in flight.  hc_workspace_bytes(n, hc, d) is the size that gives
- *   the fastest path.  When mixes is NULL the workspace is required and must
- *   hold at least the mix numbers (n * mix_hc floats, rounded up to 256
- *   bytes), which the general path keeps there between its kernels.  At
- *   hc = 8 the rest of it (or all of it when mixes is given) also takes W
- *   converted to the tensor core's bf16 hi/lo rows (4 * mix_hc * hc*d
- *   bytes); a workspace without that room, or NULL when mixes is given, is
- *   accepted and the projection then converts W inside its kernel (slower,
- *   same results bit for bit).
+ *   workspace: device scratch (nullable), 256-byte aligned, not shared with
+ *   another call in flight.  hc_workspace_bytes(n, hc, d) is a size that
+ *   serves every path.  What reads it:
+ *     - the decode and fused paths (hc = 4 with d % 256 == 0, d <= 5120, on
+ *       the shapes and token counts they take) read none of it: NULL, or
+ *       any size, is accepted there;
+ *     - the general path (every other shape) keeps the mix numbers there
+ *       when mixes is NULL: the workspace must then hold at least n * mix_hc
+ *       floats (rounded up to 256 bytes), else HC_ERR_INVALID_ARG (or
+ *       HC_ERR_MISALIGNED), returned before anything is enqueued;
+ *     - at hc = 8 the general path also puts W converted to the tensor
+ *       core's bf16 hi/lo rows (4 * mix_hc * hc*d bytes) past the mix numbers
+ *       (at its start when mixes is given); a workspace without that room is
+ *       accepted and the projection then converts W inside its kernel
+ *       (slower, same results bit for bit).
  */
 hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps,
                        float norm_eps, const uint16_t *x, const float *w_mix,
@@ -163,10 +168,12 @@ hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
                             void *workspace, size_t workspace_bytes,
                             hc_stream_t stream);
 
-/* Scratch bytes for hc_mixes_pre(_norm) at these sizes: n * mix_hc floats
- * rounded up to 256 bytes, plus at hc = 8 the converted W (4 * mix_hc * hc*d
- * bytes, rounded up to 256); 0 for n == 0 or invalid sizes.  Pure host
- * function; the value depends only on its arguments. */
+/* Scratch bytes for hc_mixes_pre(_norm) at these sizes, enough for whichever
+ * path the call takes: n * mix_hc floats rounded up to 256 bytes, plus at
+ * hc = 8 the converted W (4 * mix_hc * hc*d bytes, rounded up to 256); 0 for
+ * n == 0 or invalid sizes.  Paths that read less (the decode and fused paths
+ * read nothing) accept a smaller workspace or NULL, as hc_mixes_pre states.
+ * Pure host function; the value depends only on its arguments. */
 size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
 
 /*
@@ -202,10 +209,14 @@ hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream);
  * buffers, a framework capturing a region into a CUDA graph where allocation
  * is forbidden, an allocator's own callbacks, or a real-time loop that must
  * never reach the allocator.  hc_mixes_pre needs a workspace for the mix
- * numbers when the caller does not want them; this call keeps them instead in
- * a fixed array compiled into the library (HC_NOALLOC_SCRATCH_FLOATS floats),
- * and otherwise computes what hc_mixes_pre computes with mixes == NULL, always
- * with the general three-kernel path (projection, split/Sinkhorn, collapse).
+ * numbers when the caller does not want them and the shape takes its general
+ * path; this call keeps them instead in a fixed array compiled into the
+ * library (HC_NOALLOC_SCRATCH_FLOATS floats), and otherwise runs what
+ * hc_mixes_pre's general path runs with mixes == NULL: the projection (on the
+ * tensor cores where they take the shape, converting W inside the kernel,
+ * else on the CUDA cores), split/Sinkhorn, and the collapse.  Its results
+ * equal those of hc_mixes_pre on that path; on the decode and fused paths
+ * hc_mixes_pre agrees with it within the library's tolerances.
  *
  * Arguments, layouts and validation are those of hc_mixes_pre without mixes
  * and workspace.  n * (2+hc)*hc must not exceed HC_NOALLOC_SCRATCH_FLOATS
@@ -213,9 +224,10 @@ hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream);
  * HC_ERR_UNSUPPORTED before anything is enqueued.  The call allocates and
  * frees nothing.
  *
- * The first call on a device looks up the device address of the array on the
- * current device (cudaGetSymbolAddress), so make that first call before any
- * stream capture.  All calls share the one array per device: calls that
+ * The first call on a device (and the first after the device's context was
+ * recreated, e.g. by cudaDeviceReset) looks up the device address of the array
+ * on the current device (cudaGetSymbolAddress), so make that first call before
+ * any stream capture.  All calls share the one array per device: calls that
  * overlap on the GPU (different streams, or unordered work from different
  * threads) race on it and must be ordered by the caller.  Each call writes
  * every scratch element it reads, so nothing needs clearing between calls.

@@ -59,21 +59,48 @@ cudaError_t launch_projection(int64_t n, int hc, int64_t d, float norm_eps, cons
     return launch_mixes(n, hc, d, norm_eps, x, w, mixes, di, s);
 }
 
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    if (get_cur == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (get_cur(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 cudaError_t device_info(DeviceInfo *out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_have[dev]) {
+    if (!g_have[dev] || ctx == 0 || g_info[dev].ctx != ctx) {
         DeviceInfo di;
         di.device = dev;
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         void *p = nullptr;
+        // (also makes the device's primary context current when it was not)
         e = cudaGetSymbolAddress(&p, g_err_word);
         if (e != cudaSuccess) return e;
         di.err_word = static_cast<unsigned int *>(p);
+        di.ctx = current_context_id();
         g_info[dev] = di;
         g_have[dev] = true;
     }
@@ -289,21 +316,30 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
                   {rng(x, n * F * 2), rng(w_mix, mix * F * 4), rng(hc_scale, 12),
                    rng(hc_base, mix * 4), rrms}))
         return HC_ERR_INVALID_ARG;
-    // Without `mixes` the workspace must be there (the general path keeps
-    // the mix numbers in it between its stages).
+    // Without `mixes` the general path keeps the mix numbers in the workspace
+    // between its stages; the decode and fused paths read no workspace.  The
+    // status a missing or unusable workspace gives on the general path, or
+    // HC_OK when it is usable.
     float *m = mixes;
+    hc_status ws_status = HC_OK;
     if (m == nullptr) {
-        if (workspace == nullptr || workspace_bytes < mix_part_bytes(n, hc))
-            return HC_ERR_INVALID_ARG;
-        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HC_ERR_MISALIGNED;
-        m = static_cast<float *>(workspace);
-        const Range rw = rng(workspace, workspace_bytes);
-        if (!disjoint({rw}, {rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
-                             rng(comb, n * (uint64_t)hc * hc * 4ull),
-                             rng(y, (uint64_t)n * d * 2), rng(x, n * F * 2),
-                             rng(w_mix, mix * F * 4), rng(hc_scale, 12), rng(hc_base, mix * 4),
-                             rrms}))
-            return HC_ERR_INVALID_ARG;
+        if (workspace == nullptr || workspace_bytes < mix_part_bytes(n, hc)) {
+            ws_status = HC_ERR_INVALID_ARG;
+        } else if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) {
+            ws_status = HC_ERR_MISALIGNED;
+        } else if (!disjoint({rng(workspace, workspace_bytes)},
+                             {rng(pre, n * hc * 4ull), rng(post, n * hc * 4ull),
+                              rng(comb, n * (uint64_t)hc * hc * 4ull),
+                              rng(y, (uint64_t)n * d * 2), rng(x, n * F * 2),
+                              rng(w_mix, mix * F * 4), rng(hc_scale, 12),
+                              rng(hc_base, mix * 4), rrms})) {
+            ws_status = HC_ERR_INVALID_ARG;
+        } else {
+            m = static_cast<float *>(workspace);
+        }
+        // Shapes that only the general path takes are settled here, before
+        // any CUDA call; the others once the path is known.
+        if (ws_status != HC_OK && !(hc == 4 && d % 256 == 0 && d <= 5120)) return ws_status;
     }
     hc::DeviceInfo di;
     if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
@@ -328,6 +364,7 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
     // workspace with room past the mix numbers (hc_workspace_bytes) also
     // takes the converted W; one that is smaller, misaligned or overlapping
     // is simply not used for it.
+    if (ws_status != HC_OK) return ws_status;
     uint16_t *wconv = nullptr;
     const uint64_t wcb = hc::mixtc_wconv_bytes(hc, d);
     if (wcb != 0 && workspace != nullptr &&

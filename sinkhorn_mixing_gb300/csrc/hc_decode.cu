@@ -374,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
 
 struct DevState {
     bool init = false;
+    unsigned long long ctx = 0;  // the context the set-up below was done in
     bool ok = false;
     int max_clusters = 0;
 };
@@ -383,8 +384,10 @@ DevState g_dec[64];
 const DevState &dec_state(const DeviceInfo &di) {
     std::lock_guard<std::mutex> lk(g_dmu);
     DevState &st = g_dec[di.device];
-    if (st.init) return st;
+    if (st.init && st.ctx == di.ctx) return st;
+    st = DevState();
     st.init = true;
+    st.ctx = di.ctx;
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only

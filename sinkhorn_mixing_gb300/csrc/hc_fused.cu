@@ -624,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct DevState {
     bool init = false;
+    unsigned long long ctx = 0;  // the context the set-up below was done in
     bool ok = false;
     int max_clusters = 0;
 };
@@ -646,8 +647,10 @@ FusedKernel kernel_for(int ncc) {
 const DevState &dev_state(const DeviceInfo &di) {
     std::lock_guard<std::mutex> lk(g_fmu);
     DevState &st = g_dev[di.device];
-    if (st.init) return st;
+    if (st.init && st.ctx == di.ctx) return st;
+    st = DevState();
     st.init = true;
+    st.ctx = di.ctx;
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only

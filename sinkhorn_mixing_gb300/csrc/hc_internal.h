@@ -12,10 +12,20 @@ namespace hc {
 struct DeviceInfo {
     int device;
     int sms;
+    unsigned long long ctx;  // unique id of the CUDA context the values below belong to
     unsigned int *err_word;  // device address of this device's error word
 };
 
-// Current device's SM count and error-word address (cached per device).
+// Unique id (cuCtxGetId) of the calling thread's current CUDA context, or 0
+// when none is current.  Ids are never reused within a process, so a cache
+// keyed on it is rebuilt after the device's context is destroyed and
+// recreated (cudaDeviceReset), when module addresses and function attributes
+// are new.
+unsigned long long current_context_id();
+
+// Current device's SM count and error-word address, cached per device and
+// context.  Per-device kernel set-up elsewhere compares its recorded ctx with
+// DeviceInfo::ctx and redoes itself when they differ.
 cudaError_t device_info(DeviceInfo *out);
 
 // Path override for tests and diagnosis, read from the environment at each

@@ -449,6 +449,7 @@ __global__ void __launch_bounds__(Cfg<HC, PRE>::kThreads, 1)
 
 struct DevState {
     bool init = false;
+    unsigned long long ctx = 0;  // the context the set-up below was done in
     bool ok = false;
 };
 std::mutex g_mmu;
@@ -463,8 +464,10 @@ bool set_attrs() {
 const DevState &mix_state(const DeviceInfo &di) {
     std::lock_guard<std::mutex> lk(g_mmu);
     DevState &st = g_mix[di.device];
-    if (st.init) return st;
+    if (st.init && st.ctx == di.ctx) return st;
+    st = DevState();
     st.init = true;
+    st.ctx = di.ctx;
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only

@@ -1,7 +1,7 @@
 // hc_noalloc.cu -- hc_mixes_pre_noalloc: the general three-kernel path of
-// hc_mixes_pre (projection -> split/Sinkhorn -> collapse) with its mix-number
-// scratch held in a fixed device array compiled into the library, for callers
-// that cannot allocate device memory.
+// hc_mixes_pre (tensor-core projection -> split/Sinkhorn -> collapse) with its
+// mix-number scratch held in a fixed device array compiled into the library,
+// for callers that cannot allocate device memory.
 //
 // Who needs this: code that runs where cudaMalloc is not allowed or not
 // available -- inside a region being captured into a CUDA graph by a framework
@@ -29,23 +29,26 @@ static __device__ __align__(256) float g_mix_scratch[HC_NOALLOC_SCRATCH_FLOATS];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float *g_scratch_ptr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name is only a host-side stand-in, so the address must come
-// from cudaGetSymbolAddress, once per device, with that device current.
-cudaError_t scratch_on_current_device(float **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+// from cudaGetSymbolAddress, with that device current.  It is looked up once
+// per device and CUDA context (di.ctx, unique in the process): after a
+// cudaDeviceReset the module is loaded anew and the address is looked up
+// again.
+cudaError_t scratch_on_current_device(const DeviceInfo &di, float **out) {
+    if (di.device < 0 || di.device >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
+    if (g_scratch_ptr[di.device] == nullptr || di.ctx == 0 ||
+        g_scratch_ctx[di.device] != di.ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_mix_scratch);
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_mix_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = static_cast<float *>(p);
+        g_scratch_ptr[di.device] = static_cast<float *>(p);
+        g_scratch_ctx[di.device] = di.ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch_ptr[di.device];
     return cudaSuccess;
 }
 
@@ -97,12 +100,15 @@ extern "C" hc_status hc_mixes_pre_noalloc(int64_t n, int hc, int64_t d, int iter
         for (const hc::Span &b : ins)
             if (hc::overlap(outs[a], b)) return HC_ERR_INVALID_ARG;
     }
-    float *scratch = nullptr;
-    if (hc::scratch_on_current_device(&scratch) != cudaSuccess) return HC_ERR_CUDA;
     hc::DeviceInfo di;
     if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    float *scratch = nullptr;
+    if (hc::scratch_on_current_device(di, &scratch) != cudaSuccess) return HC_ERR_CUDA;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = hc::launch_mixes(n, hc, d, norm_eps, x, w_mix, scratch, di, s);
+    // the projection hc_mixes_pre's general path uses (tensor cores where
+    // they take the shape), with W converted inside the kernel: no scratch
+    // beyond the mix numbers
+    cudaError_t e = hc::launch_projection(n, hc, d, norm_eps, x, w_mix, scratch, nullptr, di, s);
     if (e == cudaSuccess)
         e = hc::launch_split_sinkhorn(n, hc, iters, eps, scratch, hc_scale, hc_base, pre, post,
                                       comb, di, s);

@@ -11,6 +11,7 @@ import torch
 import oracle
 from oracle import compare
 from sinkhorn_mixing_gb300 import inputs
+from parity import check_mixes_all, check_pre_all, check_split_all, oracle_mixes
 
 pytestmark = pytest.mark.gpu
 
@@ -94,14 +95,41 @@ def test_fused_mixes_only_entry(hc):
 
 
 @pytest.mark.parametrize("iters", [1, 20, 50])
-def test_fused_many_tiles_sampled(hc, iters):
+def test_fused_many_tiles_every_token(hc, iters):
+    # 625 tiles over every cluster: every tile, round and owner is compared
     n = 40000
     x, w, sc, base = case(n, 5120, seed=iters, scale_lo=1e-3, scale_hi=1e3)
     y, pre, post, comb, m = hc.hc_mixes_pre(x, w, sc, base, iters, want_mixes=True)
     torch.cuda.synchronize()
-    r = np.random.default_rng(iters)
-    idx = np.unique(np.concatenate([[0, 63, 64, n - 1], r.choice(n, 150, replace=False)]))
-    check_all(x, w, sc, base, y, pre, post, comb, m, iters, idx)
+    xb = bits(x)
+    check_mixes_all(np64(m), oracle_mixes(None, xb, w.cpu().numpy(), 1e-20))
+    check_split_all(np64(m), np64(pre), np64(post), np64(comb), sc.cpu().numpy(),
+                    base.cpu().numpy(), 4, iters, 1e-6)
+    check_pre_all(bits(y), xb, np64(pre), 4, "fused y (40,000 tokens, iters %d)" % iters)
+
+
+@pytest.mark.parametrize("n", [33, 300, 4096])
+def test_fused_and_decode_paths_take_a_null_workspace(hc, n):
+    # the decode (33 tokens) and fused (300, 4096 tokens) paths read no
+    # workspace: the C ABI accepts NULL there, with the same results as the
+    # binding's call (which passes a workspace)
+    import ctypes
+    from sinkhorn_mixing_gb300 import binding
+    os.environ.pop("HCMIX_PATH", None)  # the shape decides
+    x, w, sc, base = case(n, 5120, seed=n)
+    want = hc.hc_mixes_pre(x, w, sc, base)
+    pre = torch.empty((n, 4), device="cuda")
+    post = torch.empty((n, 4), device="cuda")
+    comb = torch.empty((n, 4, 4), device="cuda")
+    y = torch.empty((n, 5120), dtype=torch.bfloat16, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = binding.lib().hc_mixes_pre(n, 4, 5120, 20, 1e-6, 1e-20, P(x), P(w), P(sc), P(base),
+                                    None, P(pre), P(post), P(comb), P(y), None, 0,
+                                    ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, binding.status_string(st)
+    torch.cuda.synchronize()
+    for a, b in zip((y, pre, post, comb), want[:4]):
+        assert torch.equal(a, b)
 
 
 def test_fused_agrees_with_general_path(hc):

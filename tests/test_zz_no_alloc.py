@@ -17,6 +17,7 @@ import torch
 import oracle
 from oracle import compare
 from sinkhorn_mixing_gb300 import inputs
+from parity import check_mixes_all, check_pre_all, check_split_all, oracle_mixes
 
 pytestmark = pytest.mark.gpu
 
@@ -61,15 +62,16 @@ def noalloc(L, x, w, sc, base, iters=20, eps=1e-6, norm_eps=1e-20):
     return y, pre, post, comb
 
 
-@pytest.mark.parametrize("n,hc,d", [(37, 4, 64), (300, 8, 5120)])
-def test_noalloc_equals_hc_mixes_pre_on_the_general_path(L, n, hc, d):
-    # the no-allocation entry runs the general three-kernel path with the
-    # CUDA-core projection; hc_mixes_pre runs the same kernels when the path
-    # is pinned to it: same inputs, so the results are identical
+@pytest.mark.parametrize("path", ["general", "ffma"])
+@pytest.mark.parametrize("n,hc,d", [(37, 4, 64), (300, 8, 5120), (500, 4, 5120)])
+def test_noalloc_equals_hc_mixes_pre_on_the_general_path(L, n, hc, d, path):
+    # the no-allocation entry runs hc_mixes_pre's general three-kernel path
+    # (tensor-core projection, or the CUDA-core one when the path is pinned to
+    # it); hc_mixes_pre pinned to the same path gives identical results
     import os
     import sinkhorn_mixing_gb300 as m
     old = os.environ.get("HCMIX_PATH")
-    os.environ["HCMIX_PATH"] = "ffma"
+    os.environ["HCMIX_PATH"] = path
     try:
         for call, seed in enumerate((1, 2)):
             x, w, sc, base = case(n, hc, d, seed + 10 * hc)
@@ -100,6 +102,41 @@ def test_noalloc_matches_fused_entry_point_within_tolerance(L):
         torch.testing.assert_close(comb, comb2, rtol=0, atol=1e-4)
         want, _, mag = oracle.hc_pre(inputs.bf16_bits(x), pre.cpu().double().numpy())
         compare.check_bf16(inputs.bf16_bits(y), want, mag, 4, "noalloc y")
+
+
+def test_noalloc_every_token_against_the_oracle(L):
+    # 40,000 tokens (hc=4, d=5120, within the fixed scratch), two calls in a
+    # row with different inputs.  Stage parity on every token: the mix numbers
+    # of the same projection kernel (hc_mixes on the general path) against the
+    # oracle's, the call's pre/post/comb against the oracle's split + Sinkhorn
+    # of those mix numbers, and y against the oracle's collapse with the
+    # call's own pre.
+    import os
+    import sinkhorn_mixing_gb300 as m
+    n = 40000
+    old = os.environ.get("HCMIX_PATH")
+    try:
+        for seed in (21, 22):
+            x, w, sc, base = case(n, 4, 5120, seed)
+            y, pre, post, comb = noalloc(L, x, w, sc, base)
+            os.environ["HCMIX_PATH"] = "general"
+            mix = m.hc_mixes(x, w)
+            # the same kernels as the call's own stages: its coefficients follow
+            pre2, post2, comb2 = m.hc_split_sinkhorn(mix, sc, base)
+            torch.cuda.synchronize()
+            for a, b in ((pre, pre2), (post, post2), (comb, comb2)):
+                assert torch.equal(a, b)
+            xb = inputs.bf16_bits(x)
+            f64 = lambda t: t.cpu().double().numpy()  # noqa: E731
+            check_mixes_all(f64(mix), oracle_mixes(None, xb, w.cpu().numpy(), 1e-20))
+            check_split_all(f64(mix), f64(pre), f64(post), f64(comb), sc.cpu().numpy(),
+                            base.cpu().numpy(), 4, 20, 1e-6)
+            check_pre_all(inputs.bf16_bits(y), xb, f64(pre), 4, "noalloc y (call %d)" % seed)
+    finally:
+        if old is None:
+            os.environ.pop("HCMIX_PATH", None)
+        else:
+            os.environ["HCMIX_PATH"] = old
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(L):
