@@ -44,6 +44,29 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return v;
 }
 
+// Packed pairs of binary32 in one 64-bit register (lo in the low half) and
+// the two-wide FMA on them: d = a * b + d per half, each rounded once.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float sum2(uint64_t v) {
+    float lo, hi;
+    unpack2(v, lo, hi);
+    return lo + hi;
+}
+// The two bf16 of a 32-bit word as a packed pair of binary32 (exact).
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t u) {
+    return pack2(bf16lo(u), bf16hi(u));
+}
+
 // Streaming (evict-first) 16-byte global load/store.  Plain coherent loads:
 // safe also when the same kernel later writes the location (in-place post).
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }

@@ -97,21 +97,6 @@ __device__ __forceinline__ void cp_async_wait(int left) {
     }
 }
 
-// d += a * b on both halves of a packed pair of binary32 numbers.
-__device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ float sum2(uint64_t v) {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo + hi;
-}
-
 // W slice [24][4w] fp32, later reused for the lanes' partials
 __host__ __device__ constexpr size_t wreg_bytes(int w) {
     return (size_t)kMix * 4 * w * 4 > (size_t)kWarps * kPartVals * kPartStride * 4

@@ -4,8 +4,11 @@
 //
 // Work decomposition
 //   * A cluster of 16 CTAs (one per SM) is persistent over 64-token tiles.
-//     CTA r owns channels [r*w, (r+1)*w) of every copy (w = d/16), i.e.
-//     4*w of the F = 4*d features of each token.
+//     CTA r owns, in every copy, the 64-channel chunks cc*16 + r (cc <
+//     d/1024), i.e. 4*d/16 of the F = 4*d features of each token.  So at
+//     each stage the cluster reads 2 KB contiguous of every (token, copy) row
+//     (contiguous 640-byte blocks per CTA put the CTAs' 128-byte pieces of a
+//     row 640 bytes apart).
 //   * The CTA keeps its slice of W_mix resident in shared memory for the whole
 //     kernel, split into bf16 hi + lo rows (48 rows = 24 hi, 24 lo), in the
 //     128-byte-swizzled K-major layout the tensor core reads.
@@ -185,7 +188,7 @@ static_assert(kStageBytes % 1024 == 0 && kWChunkBytes % 1024 == 0, "swizzle atom
 // First feature (within the token's F) of W chunk kc = copy*ncc + cc of CTA `rank`.
 __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams &p) {
     const int j = kc / p.ncc, cc = kc % p.ncc;
-    return j * p.d + rank * (p.ncc * 64) + cc * 64;
+    return j * p.d + (cc * kCluster + rank) * 64;
 }
 
 // ---------------------------------------------------------------- kernel
@@ -229,6 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(kMmaDrain), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_expect_tx(bar(kRecvFull), kRecvTx);
+        // The first stages' loads go out now, so that their latency overlaps
+        // the W set-up below (the ring and W are disjoint).
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap))
+                     : "memory");
+        for (int q = 0; q < kSlots && q < ncc * T; ++q) {
+            mbar_expect_tx(bar(bFull(q)), kStageBytes);
+            tma_load_4d(su32(sm.ring + q * kStageBytes), &tmap, 0, (cluster + (q / ncc) * nclusters) * kTM,
+                        (q % ncc) * kCluster + rank, 0, bar(bFull(q)));
+        }
     }
     if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -237,9 +249,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp == kWarpProducer && lane == 0)
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap))
-                     : "memory");
     // W slice -> bf16 hi/lo rows in the swizzled K-major layout.  Row i < 24
     // holds hi(W[i]), row 24 + i holds lo(W[i]) = bf16(W - hi).  Each 8-float
     // piece of W is read once for both rows, with kPieces pieces in flight
@@ -324,13 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t q = (uint32_t)(ncc * it + cc);
                     const int slot = (int)(q % kSlots);
                     const uint32_t use = q / kSlots;
+                    if (q < (uint32_t)kSlots) {  // issued during the set-up
+                        last_use[slot] = 0;
+                        continue;
+                    }
                     if (!wait_bar<false>(bar(bEmpty(slot)), (use & 1) ^ 1, abort, p.err)) {
                         ok = false;
                         break;
                     }
                     mbar_expect_tx(bar(bFull(slot)), kStageBytes);
                     tma_load_4d(su32(sm.ring + slot * kStageBytes), &tmap, 0, tile * kTM,
-                                rank * ncc + cc, 0, bar(bFull(slot)));
+                                cc * kCluster + rank, 0, bar(bFull(slot)));
                     last_use[slot] = (int)use;
                 }
             }
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < T && ok; ++it) {
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            float ss = 0.f;
+            uint64_t s2[4] = {0, 0, 0, 0};  // independent packed sums: short FMA chains
             for (int cc = 0; cc < ncc; ++cc) {
                 const uint32_t q = (uint32_t)(ncc * it + cc);
                 const int slot = (int)(q % kSlots);
@@ -399,16 +412,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         // chunk (4h+m) ^ (row & 7): 8 consecutive lanes hit 8 bank groups
-                        float f[8];
-                        unpack8(lds128(base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4)), f);
+                        const uint4 v = lds128(base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4));
+                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                        for (int e = 0; e < 4; ++e) {
+                            const uint64_t xp = bf16x2_to_f32x2(wv[e]);
+                            ffma2(s2[e], xp, xp);
+                        }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
             }
             if (!ok) break;
+            float ss = (sum2(s2[0]) + sum2(s2[1])) + (sum2(s2[2]) + sum2(s2[3]));
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
             if (!__all_sync(0xFFFFFFFFu,
                             wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
