@@ -82,6 +82,15 @@ def bytes_post(n, hc, d):
     return n * (d * 2 + hc * d * 2 + (hc + hc * hc) * 4 + hc * d * 2)
 
 
+def bytes_post_mixes_pre(n, hc, d):
+    """hc_post + hc_mixes_pre in one pass: out, residual and post/comb read
+    once, the new stream written once (not read back), y and the next
+    coefficients written once, W read once."""
+    mix = (2 + hc) * hc
+    return (n * (d * 2 + hc * d * 2 + (hc + hc * hc) * 4 + hc * d * 2 + d * 2 +
+                 (2 * hc + hc * hc) * 4) + mix * hc * d * 4 + (3 + mix) * 4)
+
+
 # ------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -500,6 +509,34 @@ def pair_timing(hc, peak, dev, steps=20):
         t_post += (mid[0].elapsed_time(m1) + mid[1].elapsed_time(e1)) / 1e3
     tp = (t_mp + t_post) / steps
     b = 2 * (bytes_mixes_pre(n, H, d) + bytes_post(n, H, d))
+    # the same block with the boundary between the sublayers fused:
+    # mixes_pre(x; A) -> post_mixes_pre(out_a, x; A -> F) -> post(out_f, x1; F)
+    pre_a, post_a, comb_a, y_a = ca
+    pre_f, post_f, comb_f, y_f = cf
+
+    def block_fused():
+        hc.hc_mixes_pre(x, pa["w"], pa["hc_scale"], pa["hc_base"], 20, wl.eps, wl.norm_eps,
+                        pre=pre_a, post=post_a, comb=comb_a, y=y_a, workspace=wsp)
+        hc.hc_post_mixes_pre(out_a, x, post_a, comb_a, pf["w"], pf["hc_scale"], pf["hc_base"],
+                             20, wl.eps, wl.norm_eps, x_next=x1, pre=pre_f, post_next=post_f,
+                             comb_next=comb_f, y=y_f, workspace=wsp)
+        hc.hc_post(out_f, x1, post_f, comb_f, y=x2)
+    for _ in range(3):
+        if flush is not None:
+            flush.zero_()
+        block_fused()
+    torch.cuda.synchronize(dev)
+    t_f = 0.0
+    for _ in range(steps):
+        if flush is not None:
+            flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        block_fused()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_f += e0.elapsed_time(e1) / 1e3
+    t_f /= steps
     if hc.hc_device_error(clear=True):
         raise RuntimeError("device error word set during the pair measurement")
     return {"workload": DESCR["prefill"] + "; attention + FFN sublayers, two parameter sets",
@@ -507,8 +544,61 @@ def pair_timing(hc, peak, dev, steps=20):
             "sublayer_tokens_per_s": 2 * n / tp, "GBps": b / tp / 1e9,
             "frac_of_hbm_roofline": b / tp / 1e9 / peak,
             "hc_mixes_pre_us": 1e6 * t_mp / steps / 2, "hc_post_us": 1e6 * t_post / steps / 2,
+            "fused_boundary_us_per_pair": 1e6 * t_f, "fused_boundary_tokens_per_s": n / t_f,
             "steps": steps, "l2": "flushed before each pair" if flush is not None
             else "inputs larger than L2"}
+
+
+def fused_sublayer_timing(hc, wl, x, out, post, comb, peak, dev, reps=20):
+    """hc_post_mixes_pre on the step's inputs: sublayer s's hc_post (its
+    output `out`, the stream x, the step's post/comb) fused with hc_mixes_pre
+    of sublayer s+1 (a second parameter set), `reps` calls timed with CUDA
+    events; beside it the same two stages as separate calls."""
+    import torch
+    from sinkhorn_mixing_gb300 import inputs
+    n, H, d = x.shape[0], x.shape[1], x.shape[2]
+    p2 = inputs.make_params(wl, 1, device=dev)
+    x1 = torch.empty_like(x)
+    pre = torch.empty((n, H), device=dev)
+    post2 = torch.empty((n, H), device=dev)
+    comb2 = torch.empty((n, H, H), device=dev)
+    y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        hc.hc_post_mixes_pre(out, x, post, comb, p2["w"], p2["hc_scale"], p2["hc_base"], 20,
+                             wl.eps, wl.norm_eps, x_next=x1, pre=pre, post_next=post2,
+                             comb_next=comb2, y=y)
+
+    def separate():
+        hc.hc_post(out, x, post, comb, y=x1)
+        hc.hc_mixes_pre(x1, p2["w"], p2["hc_scale"], p2["hc_base"], 20, wl.eps, wl.norm_eps,
+                        pre=pre, post=post2, comb=comb2, y=y)
+
+    res = {}
+    for name, fn in (("fused", fused), ("separate", separate)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        launches0 = hc.hc_launch_count()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        res[name] = (a.elapsed_time(b) / 1e3 / reps,
+                     (hc.hc_launch_count() - launches0) // reps)
+    if hc.hc_device_error(clear=True):
+        raise RuntimeError("device error word set during the fused-sublayer measurement")
+    nb = bytes_post_mixes_pre(n, H, d)
+    t, nl = res["fused"]
+    ts, nls = res["separate"]
+    return {"what": "hc_post of sublayer s fused with hc_mixes_pre of sublayer s+1 "
+                    "(hc_post_mixes_pre); per call = one sublayer boundary",
+            "us_per_call": 1e6 * t, "launches_per_call": nl, "tokens_per_s": n / t,
+            "algorithmic_bytes": nb, "GBps": nb / t / 1e9, "frac": nb / t / 1e9 / peak,
+            "separate_us": 1e6 * ts, "separate_launches": nls,
+            "separate_tokens_per_s": n / ts, "speedup_vs_separate": ts / t, "reps": reps}
 
 
 def cpu_baseline(wl, seconds):
@@ -781,6 +871,7 @@ def run_ours(args, wl, ws, rank, local):
         if hc.hc_device_error(clear=True):
             raise RuntimeError("device error word set during the RMSNorm measurement")
     if not args.no_configs and n == wl.n and args.workload == "large":
+        line["fused_sublayer"] = fused_sublayer_timing(hc, wl, x, out, post, comb, peak, dev)
         line["prefill"] = workload_timing(hc, "prefill", peak, dev)
         line["prefill_pair"] = pair_timing(hc, peak, dev)
         line["stress"] = workload_timing(hc, "stress", peak, dev)

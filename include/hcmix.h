@@ -9,6 +9,8 @@
  *   hc_pre, hc_post    "Mix projection" page: Block.hc_pre, Block.hc_post
  *   hc_mixes_pre       the first three fused: what one sublayer needs before
  *                      it runs (Block docstring on the same page)
+ *   hc_post_mixes_pre  hc_post of one sublayer fused with hc_mixes_pre of the
+ *                      next (same docstring)
  *
  * Conventions shared by every entry point
  *   - Every tensor pointer is a DEVICE pointer owned by the caller.  The
@@ -166,6 +168,43 @@ hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
                             const float *rms_weight, float rms_eps, float *mixes,
                             float *pre, float *post, float *comb, uint16_t *y,
                             void *workspace, size_t workspace_bytes,
+                            hc_stream_t stream);
+
+/*
+ * hc_post_mixes_pre -- the boundary between two sublayers in one call: the
+ * expansion of sublayer s's output back into the stream, then everything the
+ * next sublayer needs from that stream ("Mix projection" page, Block
+ * docstring: each sublayer sits between hc_pre and hc_post, and the stream
+ * hc_post produces is the input of the next sublayer):
+ *   x_next = hc_post(out, residual, post, comb)              (sublayer s)
+ *   (y_next, pre_next, post_next, comb_next[, mixes])
+ *          = hc_mixes_pre(x_next; w_mix, hc_scale, hc_base)   (sublayer s+1)
+ * Each sublayer uses the coefficients computed from its own input stream.
+ * Results equal those of hc_post followed by hc_mixes_pre: x_next bit for
+ * bit; the rest up to binary32 rounding order (bit for bit where both calls
+ * take the same projection kernel).  On the fused path (hc = 4, d a multiple
+ * of 1024 up to 5120, more tokens than the decode kernel takes) it is one
+ * kernel that reads the residual once: the new stream is computed in shared
+ * memory, stored to x_next and projected from there, which saves re-reading
+ * it from HBM.
+ *   out [n, d] bf16;  residual [n, hc, d] bf16;  post [n, hc], comb [n, hc, hc]
+ *   float -- sublayer s's output and coefficients (in)
+ *   x_next [n, hc, d] bf16 (out) -- the new stream; x_next == residual (in
+ *   place) is allowed
+ *   w_mix, hc_scale, hc_base -- sublayer s+1's parameters (in)
+ *   mixes (out, may be NULL), pre_next, post_next [n, hc], comb_next
+ *   [n, hc, hc], y_next [n, d] -- as hc_mixes_pre's outputs on x_next
+ *   workspace, workspace_bytes -- as in hc_mixes_pre
+ * Every output must be disjoint from every input and from every other output
+ * (except x_next == residual); in particular pre_next/post_next/comb_next may
+ * not be the buffers that hold post/comb.
+ */
+hc_status hc_post_mixes_pre(int64_t n, int hc, int64_t d, const uint16_t *out,
+                            const uint16_t *residual, const float *post, const float *comb,
+                            uint16_t *x_next, int iters, float eps, float norm_eps,
+                            const float *w_mix, const float *hc_scale, const float *hc_base,
+                            float *mixes, float *pre_next, float *post_next, float *comb_next,
+                            uint16_t *y_next, void *workspace, size_t workspace_bytes,
                             hc_stream_t stream);
 
 /* Scratch bytes for hc_mixes_pre(_norm) at these sizes, enough for whichever

@@ -53,6 +53,8 @@ def lib():
                                    ctypes.c_size_t, P]
         L.hc_mixes_pre_norm.argtypes = [i64, i32, i64, i32, f32, f32, P, P, P, P, P, f32, P, P,
                                         P, P, P, P, ctypes.c_size_t, P]
+        L.hc_post_mixes_pre.argtypes = [i64, i32, i64, P, P, P, P, P, i32, f32, f32, P, P, P, P,
+                                        P, P, P, P, P, ctypes.c_size_t, P]
         L.hc_workspace_bytes.argtypes = [i64, i32, i64]
         L.hc_workspace_bytes.restype = ctypes.c_size_t
         L.hc_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
@@ -60,7 +62,7 @@ def lib():
         L.hc_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
         L.hc_selftest_wait_timeout.restype = i32
         for f in ("hc_mixes", "hc_split_sinkhorn", "hc_pre", "hc_post", "hc_mixes_pre",
-                  "hc_mixes_pre_norm", "hc_device_error"):
+                  "hc_mixes_pre_norm", "hc_post_mixes_pre", "hc_device_error"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -288,6 +290,52 @@ def hc_mixes_pre_norm(x, w_mix, hc_scale, hc_base, rms_weight, sinkhorn_iters: i
                  _ptr(rms_weight), float(rms_eps), _ptr(mixes), _ptr(pre), _ptr(post), _ptr(comb),
                  _ptr(y), _ptr(workspace), wbytes, _stream(dev, stream)), "hc_mixes_pre_norm")
     return y, pre, post, comb, mixes
+
+
+def hc_post_mixes_pre(out, residual, post, comb, w_mix, hc_scale, hc_base,
+                      sinkhorn_iters: int = 20, eps: float = 1e-6, norm_eps: float = 1e-20,
+                      x_next=None, want_mixes: bool = False, mixes=None, pre=None,
+                      post_next=None, comb_next=None, y=None, workspace=None, stream=None):
+    """hc_post of one sublayer and hc_mixes_pre of the next in one call:
+    x_next = hc_post(out, residual, post, comb) (x_next may be residual), then
+    the next sublayer's (y, pre, post, comb[, mixes]) from x_next with its
+    parameters w_mix, hc_scale, hc_base.
+    Returns (x_next, y, pre, post, comb, mixes-or-None)."""
+    _need(residual, "residual", torch.bfloat16)
+    dev = residual.device
+    lead, n, hc, d = _stream_dims(residual)
+    _need(out, "out", torch.bfloat16, dev)
+    if out.numel() != n * d:
+        raise ValueError("out must hold n*d values")
+    _need(post, "post", torch.float32, dev)
+    _need(comb, "comb", torch.float32, dev)
+    if post.numel() != n * hc or comb.numel() != n * hc * hc:
+        raise ValueError("post/comb sizes do not match residual")
+    mix = (2 + hc) * hc
+    _need(w_mix, "w_mix", torch.float32, dev)
+    _need(hc_scale, "hc_scale", torch.float32, dev)
+    _need(hc_base, "hc_base", torch.float32, dev)
+    x_next = _out(x_next, "x_next", lead + (hc, d), torch.bfloat16, dev)
+    if want_mixes or mixes is not None:
+        mixes = _out(mixes, "mixes", lead + (mix,), torch.float32, dev)
+    pre = _out(pre, "pre", lead + (hc,), torch.float32, dev)
+    post_next = _out(post_next, "post_next", lead + (hc,), torch.float32, dev)
+    comb_next = _out(comb_next, "comb_next", lead + (hc, hc), torch.float32, dev)
+    y = _out(y, "y", lead + (d,), torch.bfloat16, dev)
+    wbytes = 0
+    if mixes is None or hc == 8:
+        wbytes = hc_workspace_bytes(n, hc, d)
+        if workspace is None and wbytes:
+            workspace = torch.empty(wbytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _need(workspace, "workspace", torch.uint8, dev)
+        wbytes = workspace.numel()
+    _check(_call(dev, lib().hc_post_mixes_pre, n, hc, d, _ptr(out), _ptr(residual), _ptr(post),
+                 _ptr(comb), _ptr(x_next), int(sinkhorn_iters), float(eps), float(norm_eps),
+                 _ptr(w_mix), _ptr(hc_scale), _ptr(hc_base), _ptr(mixes), _ptr(pre),
+                 _ptr(post_next), _ptr(comb_next), _ptr(y), _ptr(workspace), wbytes,
+                 _stream(dev, stream)), "hc_post_mixes_pre")
+    return x_next, y, pre, post_next, comb_next, mixes
 
 
 def hc_launch_count() -> int:

@@ -412,6 +412,73 @@ hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps, 
                           workspace_bytes, stream);
 }
 
+hc_status hc_post_mixes_pre(int64_t n, int hc, int64_t d, const uint16_t *out,
+                            const uint16_t *residual, const float *post, const float *comb,
+                            uint16_t *x_next, int iters, float eps, float norm_eps,
+                            const float *w_mix, const float *hc_scale, const float *hc_base,
+                            float *mixes, float *pre_next, float *post_next, float *comb_next,
+                            uint16_t *y_next, void *workspace, size_t workspace_bytes,
+                            hc_stream_t stream) {
+    hc_status st = check_shape(n, hc, d);
+    if (st != HC_OK) return st;
+    if (iters < 1 || !finite_nonneg(eps) || !finite_nonneg(norm_eps)) return HC_ERR_INVALID_ARG;
+    if (n == 0) return HC_OK;
+    if ((st = ptrs_ok({out, residual, post, comb, x_next, w_mix, hc_scale, hc_base, pre_next,
+                       post_next, comb_next, y_next})) != HC_OK)
+        return st;
+    if (mixes != nullptr && !al16(mixes)) return HC_ERR_MISALIGNED;
+    const uint64_t mix = (uint64_t)(2 + hc) * hc, F = (uint64_t)hc * d;
+    const uint64_t xbytes = (uint64_t)n * F * 2;
+    const Range rx = rng(x_next, xbytes), rres = rng(residual, xbytes);
+    const bool in_place = (const void *)x_next == (const void *)residual;
+    if (!in_place && overlap(rx, rres)) return HC_ERR_INVALID_ARG;
+    const Range rmix = mixes ? rng(mixes, n * mix * 4) : Range{0, 0};
+    // every output disjoint from every other and from every input (x_next may
+    // be the residual itself)
+    if (!disjoint({rx, rmix, rng(pre_next, n * hc * 4ull), rng(post_next, n * hc * 4ull),
+                   rng(comb_next, n * (uint64_t)hc * hc * 4ull), rng(y_next, (uint64_t)n * d * 2)},
+                  {rng(out, (uint64_t)n * d * 2), rng(post, n * hc * 4ull),
+                   rng(comb, n * (uint64_t)hc * hc * 4ull), rng(w_mix, mix * F * 4),
+                   rng(hc_scale, 12), rng(hc_base, mix * 4)}))
+        return HC_ERR_INVALID_ARG;
+    if (!disjoint({rmix, rng(pre_next, n * hc * 4ull), rng(post_next, n * hc * 4ull),
+                   rng(comb_next, n * (uint64_t)hc * hc * 4ull), rng(y_next, (uint64_t)n * d * 2)},
+                  {rres}))
+        return HC_ERR_INVALID_ARG;
+    hc::DeviceInfo di;
+    if (hc::device_info(&di) != cudaSuccess) return HC_ERR_CUDA;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (hc::fused_supported(hc, d, di) && !hc::decode_supported(n, hc, d, di)) {
+        // one launch: the ring streams the residual; the new stream goes to
+        // x_next and is projected, normalised and collapsed on the way
+        return from_cuda(hc::launch_fused_post(n, hc, d, out, residual, post, comb, x_next,
+                                               iters, eps, norm_eps, w_mix, hc_scale, hc_base,
+                                               mixes, pre_next, post_next, comb_next, y_next, di,
+                                               s));
+    }
+    // other shapes and few tokens: hc_post, then hc_mixes_pre on its result.
+    // hc_mixes_pre's workspace rule is checked here, before the first launch:
+    // its general path keeps the mix numbers in the workspace.
+    if (mixes == nullptr && !hc::decode_supported(n, hc, d, di) &&
+        !hc::fused_supported(hc, d, di)) {
+        if (workspace == nullptr || workspace_bytes < mix_part_bytes(n, hc))
+            return HC_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return HC_ERR_MISALIGNED;
+        if (!disjoint({rng(workspace, workspace_bytes)},
+                      {rx, rres, rng(out, (uint64_t)n * d * 2), rng(post, n * hc * 4ull),
+                       rng(comb, n * (uint64_t)hc * hc * 4ull), rng(w_mix, mix * F * 4),
+                       rng(hc_scale, 12), rng(hc_base, mix * 4), rng(pre_next, n * hc * 4ull),
+                       rng(post_next, n * hc * 4ull), rng(comb_next, n * (uint64_t)hc * hc * 4ull),
+                       rng(y_next, (uint64_t)n * d * 2)}))
+            return HC_ERR_INVALID_ARG;
+    }
+    const cudaError_t e = hc::launch_post(n, hc, d, out, residual, post, comb, x_next, di, s);
+    if (e != cudaSuccess) return HC_ERR_CUDA;
+    return mixes_pre_impl(n, hc, d, iters, eps, norm_eps, x_next, w_mix, hc_scale, hc_base,
+                          nullptr, 0.0f, mixes, pre_next, post_next, comb_next, y_next, workspace,
+                          workspace_bytes, stream);
+}
+
 hc_status hc_selftest_wait_timeout(uint64_t limit_ns, hc_stream_t stream) {
     if (limit_ns < 1 || limit_ns > 1000000000ull) return HC_ERR_INVALID_ARG;
     hc::DeviceInfo di;

@@ -112,6 +112,13 @@ struct FusedParams {
     float *comb;
     uint16_t *y;
     unsigned int *err;
+    // hc_post of the previous sublayer (POST variant only): the ring streams
+    // the residual, and the stream x that the projection, the squares and
+    // the collapse see is x_next = hc_post(out, residual, post_in, comb_in)
+    const uint16_t *out;
+    const float *post_in;
+    const float *comb_in;
+    uint16_t *x_next;
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -148,7 +155,8 @@ constexpr int kRecvFree = 2 * kSlots + 9;
 __host__ __device__ constexpr int bPreReady(int i) { return 2 * kSlots + 10 + i; }
 __host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 10 + kColDoneBufs + i; }
 constexpr int kMmaDrain = 2 * kSlots + 10 + 2 * kColDoneBufs;
-constexpr int kNumBars = kMmaDrain + 1;
+__host__ __device__ constexpr int bPostDone(int s) { return kMmaDrain + 1 + s; }
+constexpr int kNumBars = kMmaDrain + 1 + kSlots;
 // Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
 constexpr int kEmptyArrivals = 5;
 
@@ -195,7 +203,7 @@ __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams
 
 // NCC = w / 64 (64-channel sub-tiles per copy per CTA) is a template
 // parameter so that all index arithmetic is by constants.
-template <int NCC>
+template <int NCC, bool POST>
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap tmap, const FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -230,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bColDone(i)), kCollapseWarps);
         }
         mbar_init(bar(kMmaDrain), 1);
+        for (int s = 0; s < kSlots; ++s) mbar_init(bar(bPostDone(s)), 4);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_expect_tx(bar(kRecvFull), kRecvTx);
         // The first stages' loads go out now, so that their latency overlaps
@@ -364,7 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < ncc; ++cc) {
                     const uint32_t q = (uint32_t)(ncc * it + cc);
                     const int slot = (int)(q % kSlots);
-                    if (!wait_bar<false>(bar(bFull(slot)), (q / kSlots) & 1, abort, p.err)) {
+                    // with POST the square warps first turn the residual stage
+                    // into the new stream in place
+                    if (!wait_bar<false>(bar(POST ? bPostDone(slot) : bFull(slot)), (q / kSlots) & 1,
+                                         abort, p.err)) {
                         ok = false;
                         break;
                     }
@@ -390,14 +402,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
         // Sums of squares: warp 2+g covers tokens 16g..16g+15 of every stage;
-        // lane -> token 16g + lane/2, half lane%2 of each 128-byte row.
+        // lane -> token 16g + lane/2, half lane%2 of each 128-byte row.  With
+        // POST these warps also compute the new stream (hc_post) first.
         const int i = 16 * (warp - kWarpSq0) + (lane >> 1);
         const int h = lane & 1;
+        auto tile_of = [&](uint32_t q) { return cluster + (int)(q / ncc) * nclusters; };
+        // POST: the sublayer output's 32 channels of this thread's row for
+        // stage q, loaded one stage ahead; the token's post and comb per tile
+        uint4 onext[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                          make_uint4(0, 0, 0, 0)};
+        auto prefetch_out = [&](uint32_t q) {
+            if (!POST || q >= (uint32_t)(ncc * T)) return;
+            const int64_t tok = (int64_t)tile_of(q) * kTM + i;
+            if (tok >= p.n) {
+#pragma unroll
+                for (int m = 0; m < 4; ++m) onext[m] = make_uint4(0, 0, 0, 0);
+                return;
+            }
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.out + tok * (int64_t)p.d + (int)(q % ncc) * (kCluster * 64) + rank * 64 + 32 * h);
+#pragma unroll
+            for (int m = 0; m < 4; ++m) onext[m] = ld_stream(src + m);
+        };
+        float po[4] = {0.f, 0.f, 0.f, 0.f}, cmf[4][4];  // the token's post and comb
+        prefetch_out(0);
         bool ok = true;
         for (int it = 0; it < T && ok; ++it) {
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
             uint64_t s2[4] = {0, 0, 0, 0};  // independent packed sums: short FMA chains
+            if (POST) {
+                const int64_t tok = (int64_t)tile_of((uint32_t)(ncc * it)) * kTM + i;
+                float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), cv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cv[j] = pv;
+                if (tok < p.n) {
+                    pv = __ldg(reinterpret_cast<const float4 *>(p.post_in) + tok);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        cv[j] = __ldg(reinterpret_cast<const float4 *>(p.comb_in) + tok * 4 + j);
+                }
+                po[0] = pv.x, po[1] = pv.y, po[2] = pv.z, po[3] = pv.w;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    cmf[j][0] = cv[j].x, cmf[j][1] = cv[j].y, cmf[j][2] = cv[j].z, cmf[j][3] = cv[j].w;
+            }
             for (int cc = 0; cc < ncc; ++cc) {
                 const uint32_t q = (uint32_t)(ncc * it + cc);
                 const int slot = (int)(q % kSlots);
@@ -407,24 +456,98 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t base = su32(sm.ring + slot * kStageBytes) + i * 128;
+                // 16-byte piece m (8 channels) of copy j of this thread's row,
+                // 128-byte swizzle: 8 consecutive lanes hit 8 bank groups
+                auto piece = [&](int j, int m) -> uint32_t {
+                    return base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4);
+                };
+                // squares in the order (piece, copy): the same order in both
+                // variants, so that they give the same sums
+                if (!POST) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                    for (int m = 0; m < 4; ++m)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 v = lds128(piece(j, m));
+                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint64_t xp = bf16x2_to_f32x2(wv[e]);
+                                ffma2(s2[e], xp, xp);
+                            }
+                        }
+                } else {
+                    // hc_post ("Mix projection" page, Block.hc_post) of this
+                    // thread's 32 channels of the stage, one 8-channel piece
+                    // at a time: x'_k = post_k out + sum_j comb[j][k] x_j, the
+                    // product first, then the copies j = 0..3 in order (as
+                    // hc_post); written back over the residual in the slot
+                    // (all four input copies of a piece are read before any is
+                    // written) and to x_next.
+                    const uint4 ocur[4] = {onext[0], onext[1], onext[2], onext[3]};
+                    prefetch_out(q + 1);
+                    const int64_t tok = (int64_t)tile_of(q) * kTM + i;
+                    const int ch0 = cc * (kCluster * 64) + rank * 64 + 32 * h;
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        // chunk (4h+m) ^ (row & 7): 8 consecutive lanes hit 8 bank groups
-                        const uint4 v = lds128(base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4));
-                        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                        // the piece's inputs as packed binary32 pairs, once
+                        uint64_t xp[4][4], op[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint64_t xp = bf16x2_to_f32x2(wv[e]);
-                            ffma2(s2[e], xp, xp);
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 v = lds128(piece(j, m));
+                            xp[j][0] = bf16x2_to_f32x2(v.x);
+                            xp[j][1] = bf16x2_to_f32x2(v.y);
+                            xp[j][2] = bf16x2_to_f32x2(v.z);
+                            xp[j][3] = bf16x2_to_f32x2(v.w);
+                        }
+                        op[0] = bf16x2_to_f32x2(ocur[m].x);
+                        op[1] = bf16x2_to_f32x2(ocur[m].y);
+                        op[2] = bf16x2_to_f32x2(ocur[m].z);
+                        op[3] = bf16x2_to_f32x2(ocur[m].w);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            uint64_t acc2[4];
+                            const uint64_t pk = pack2(po[k], po[k]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                acc2[e] = 0x8000000080000000ull;  // -0: the product alone
+                                ffma2(acc2[e], pk, op[e]);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const uint64_t cmk = pack2(cmf[j][k], cmf[j][k]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) ffma2(acc2[e], cmk, xp[j][e]);
+                            }
+                            uint32_t nw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                float lo, hi;
+                                unpack2(acc2[e], lo, hi);
+                                nw[e] = pack_bf16x2(lo, hi);
+                                const uint64_t xq = bf16x2_to_f32x2(nw[e]);
+                                ffma2(s2[e], xq, xq);
+                            }
+                            const uint4 nv = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                            sts128(piece(k, m), nv);
+                            if (tok < p.n)
+                                st_stream(reinterpret_cast<uint4 *>(
+                                              p.x_next + (tok * 4 + k) * (int64_t)p.d + ch0 + 8 * m),
+                                          nv);
                         }
                     }
+                    // the new stream in the slot, for the tensor core (async proxy)
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bPostDone(slot)));
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
             }
             if (!ok) break;
+            // POST: the tile's x_next is visible GPU-wide before its records
+            // (and so before any owner's collapse re-reads it)
+            if (POST) __threadfence();
             float ss = (sum2(s2[0]) + sum2(s2[1])) + (sum2(s2[2]) + sum2(s2[3]));
             ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
             if (!__all_sync(0xFFFFFFFFu,
@@ -650,14 +773,15 @@ DevState g_dev[64];
 
 using FusedKernel = void (*)(CUtensorMap, FusedParams);
 
-// The instantiation for w = 64 * ncc channels per CTA.
-FusedKernel kernel_for(int ncc) {
+// The instantiation for w = 64 * ncc channels per CTA (POST: with the
+// previous sublayer's hc_post in front).
+FusedKernel kernel_for(int ncc, bool post) {
     switch (ncc) {
-        case 1: return k_fused<1>;
-        case 2: return k_fused<2>;
-        case 3: return k_fused<3>;
-        case 4: return k_fused<4>;
-        default: return k_fused<5>;
+        case 1: return post ? k_fused<1, true> : k_fused<1, false>;
+        case 2: return post ? k_fused<2, true> : k_fused<2, false>;
+        case 3: return post ? k_fused<3, true> : k_fused<3, false>;
+        case 4: return post ? k_fused<4, true> : k_fused<4, false>;
+        default: return post ? k_fused<5, true> : k_fused<5, false>;
     }
 }
 
@@ -672,14 +796,15 @@ const DevState &dev_state(const DeviceInfo &di) {
     if (cudaGetDeviceProperties(&prop, di.device) != cudaSuccess) return st;
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
     if (tensor_map_encoder() == nullptr) return st;
-    for (int ncc = 1; ncc <= kMaxNcc; ++ncc) {
-        if (cudaFuncSetAttribute(kernel_for(ncc), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem_bytes(ncc)) != cudaSuccess)
-            return st;
-        if (cudaFuncSetAttribute(kernel_for(ncc), cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                 1) != cudaSuccess)
-            return st;
-    }
+    for (int ncc = 1; ncc <= kMaxNcc; ++ncc)
+        for (int post = 0; post < 2; ++post) {
+            if (cudaFuncSetAttribute(kernel_for(ncc, post), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)smem_bytes(ncc)) != cudaSuccess)
+                return st;
+            if (cudaFuncSetAttribute(kernel_for(ncc, post),
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+                return st;
+        }
     const size_t smem = smem_bytes(kMaxNcc);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kCluster);
@@ -693,7 +818,7 @@ const DevState &dev_state(const DeviceInfo &di) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int nc = 0;
-    if (cudaOccupancyMaxActiveClusters(&nc, kernel_for(kMaxNcc), &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&nc, kernel_for(kMaxNcc, true), &cfg) != cudaSuccess) {
         cudaGetLastError();
         return st;
     }
@@ -712,12 +837,19 @@ bool fused_supported(int hc, int64_t d, const DeviceInfo &di) {
     return dev_state(di).ok;
 }
 
-cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
-                         const uint16_t *x, const float *w, const float *scale,
-                         const float *base, float *mixes, float *pre, float *post, float *comb,
-                         uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+namespace {
+
+// ring_src: the tensor the ring streams (x, or the residual with POST);
+// x: the stream the collapse re-reads (x, or x_next with POST).
+cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_eps,
+                        const uint16_t *ring_src, const uint16_t *x, const float *w,
+                        const float *scale, const float *base, float *mixes, float *pre,
+                        float *post, float *comb, uint16_t *y, const uint16_t *out,
+                        const float *post_in, const float *comb_in, uint16_t *x_next,
+                        const DeviceInfo &di, cudaStream_t s) {
     const DevState &st = dev_state(di);
-    if (!st.ok || hc != 4 || n >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+    if (!st.ok || n >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+    const bool with_post = out != nullptr;
     const int64_t F = 4 * d;
     const int ncc = (int)(d / (kCluster * 64));
     // 4-D view of x: {64 channels, token, 64-channel chunk of a copy, copy};
@@ -729,7 +861,7 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     const cuuint32_t box[4] = {64, kTM, 1, 4};
     const cuuint32_t estride[4] = {1, 1, 1, 1};
     CUresult r = tensor_map_encoder()(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                             const_cast<uint16_t *>(x), gdim, gstride, box, estride,
+                             const_cast<uint16_t *>(ring_src), gdim, gstride, box, estride,
                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -754,6 +886,10 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     p.comb = comb;
     p.y = y;
     p.err = di.err_word;
+    p.out = out;
+    p.post_in = post_in;
+    p.comb_in = comb_in;
+    p.x_next = x_next;
     const int nclusters = p.num_tiles < st.max_clusters ? p.num_tiles : st.max_clusters;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
@@ -767,9 +903,31 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc), tmap, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc, with_post), tmap, p);
     if (e != cudaSuccess) return e;
     return launched();
+}
+
+}  // namespace
+
+cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                         const uint16_t *x, const float *w, const float *scale,
+                         const float *base, float *mixes, float *pre, float *post, float *comb,
+                         uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+    if (hc != 4) return cudaErrorNotSupported;
+    return launch_impl(n, d, iters, eps, norm_eps, x, x, w, scale, base, mixes, pre, post, comb,
+                       y, nullptr, nullptr, nullptr, nullptr, di, s);
+}
+
+cudaError_t launch_fused_post(int64_t n, int hc, int64_t d, const uint16_t *out,
+                              const uint16_t *residual, const float *post_in,
+                              const float *comb_in, uint16_t *x_next, int iters, float eps,
+                              float norm_eps, const float *w, const float *scale,
+                              const float *base, float *mixes, float *pre, float *post,
+                              float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+    if (hc != 4 || pre == nullptr) return cudaErrorNotSupported;
+    return launch_impl(n, d, iters, eps, norm_eps, residual, x_next, w, scale, base, mixes, pre,
+                       post, comb, y, out, post_in, comb_in, x_next, di, s);
 }
 
 }  // namespace hc

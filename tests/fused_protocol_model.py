@@ -12,7 +12,9 @@ the kernel's roles as generators that yield the barrier waits they make:
             order and releases each slot by a commit (commits complete in
             issue order), then commits acc_full;
   sq (x4)   consume every stage in order, release it, publish the tile's sums
-            of squares through sq_full / sq_empty;
+            of squares through sq_full / sq_empty; with `post` they first
+            rewrite the stage in place (hc_post of the previous sublayer) and
+            signal post_done, which the MMA waits for instead of full;
   epi (x2)  read the accumulator and the squares, wait until the previous
             tile's records were read (recv_free), then send their records to
             the owners, whose recv_full they complete by bytes;
@@ -79,10 +81,11 @@ STEP = ("step",)
 
 
 def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_only=False,
-             seed=0, mutation=None):
+             seed=0, mutation=None, post=False):
     """Run one random interleaving; raises ProtocolError on any violation.
     `mutation` plants a known protocol mistake (for the tests that show the
-    model can fail): "release_before_read", "empty_parity"."""
+    model can fail): "release_before_read", "empty_parity", "mma_waits_full"
+    (with post)."""
     rnd = random.Random(seed)
     events = []
 
@@ -94,6 +97,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
     for r in range(C):
         cs.append(dict(
             full=[Barrier("full", 1) for _ in range(S)],
+            post_done=[Barrier("post_done", 4) for _ in range(S)],
+            posted=[set() for _ in range(S)],
             empty=[Barrier("empty", 5) for _ in range(S)],  # MMA commit + 4 square warps
             slot=[None] * S, holders=[set() for _ in range(S)],
             acc_full=[Barrier("acc_full", 1) for _ in range(2)],
@@ -126,6 +131,7 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                     if c["holders"][s]:
                         raise ProtocolError("a load lands in a slot that is being read")
                     c["slot"][s] = q
+                    c["posted"][s] = set()
                     c["full"][s].complete_tx(1)
                 later(land)
 
@@ -148,9 +154,12 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             for st in range(NS):
                 q = NS * it + st
                 s = q % S
-                yield wait(c["full"][s], (q // S) & 1)
+                waits_post = post and mutation != "mma_waits_full"
+                yield wait(c["post_done" if waits_post else "full"][s], (q // S) & 1)
                 if c["slot"][s] != q:
                     raise ProtocolError("MMA wants stage %d, slot holds %s" % (q, c["slot"][s]))
+                if post and len(c["posted"][s]) != 4:
+                    raise ProtocolError("MMA reads stage %d before it was rewritten" % q)
                 c["holders"][s].add("mma")
                 chain.append(("empty", s, None))
                 later(commit)
@@ -168,6 +177,9 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                     raise ProtocolError("squares want stage %d, slot holds %s" % (q, c["slot"][s]))
                 c["holders"][s].add(w)
                 yield STEP
+                if post:
+                    c["posted"][s].add(w)
+                    c["post_done"][s].arrive()
                 c["holders"][s].discard(w)
                 c["empty"][s].arrive()
             yield wait(c["sq_empty"][b], ((it >> 1) & 1) ^ 1)

@@ -168,3 +168,34 @@ def test_workspace_rules(L):
         assert mixes_pre_call(L, d=5120) == CUDA
         assert mixes_pre_call(L, d=1024, ws=fake(9), wsb=16) == CUDA
         assert mixes_pre_call(L, d=256) == CUDA
+
+
+def post_mixes_pre_call(L, n=4, hc=4, d=64, iters=20, x_next=None, pre=None, mixes=None, ws=None,
+                        wsb=0):
+    # out, residual, post, comb | x_next | w, scale, base | mixes, pre, post', comb', y
+    args = [fake(0), fake(1), fake(2), fake(3), fake(4) if x_next is None else x_next, iters,
+            1e-6, 1e-20, fake(5), fake(6), fake(7), mixes, fake(8) if pre is None else pre,
+            fake(9), fake(10), fake(11), ws, wsb, None]
+    return L.hc_post_mixes_pre(n, hc, d, *args)
+
+
+def test_post_mixes_pre_validation(L):
+    # n == 0 is a no-op even with null pointers
+    assert L.hc_post_mixes_pre(0, 4, 64, *([None] * 5), 20, 1e-6, 1e-20, *([None] * 8), None, 0,
+                               None) == OK
+    assert post_mixes_pre_call(L, hc=3) == UNSUPPORTED
+    assert post_mixes_pre_call(L, d=12) == MISALIGNED
+    assert post_mixes_pre_call(L, iters=0) == INVALID
+    assert post_mixes_pre_call(L, x_next=ctypes.c_void_p(0)) == INVALID
+    assert post_mixes_pre_call(L, pre=fake(8, 4)) == MISALIGNED
+    assert post_mixes_pre_call(L, mixes=fake(12, 8)) == MISALIGNED
+    # x_next partly over the residual; the new coefficients over the old ones;
+    # an output over the sublayer output
+    assert post_mixes_pre_call(L, x_next=fake(1, 16)) == INVALID
+    assert post_mixes_pre_call(L, pre=fake(2)) == INVALID
+    assert post_mixes_pre_call(L, pre=fake(0, 32)) == INVALID
+    # pre_next over the residual, with x_next in place
+    assert post_mixes_pre_call(L, x_next=fake(1), pre=fake(1, 64)) == INVALID
+    if NO_GPU:
+        # in place (x_next == residual) passes validation
+        assert post_mixes_pre_call(L, x_next=fake(1)) == CUDA

@@ -17,6 +17,20 @@ def test_kernel_configuration_runs_clean(stages, mixes_only):
                  mixes_only=mixes_only, seed=seed)
 
 
+@pytest.mark.parametrize("stages", [1, 3, 5])
+def test_post_variant_runs_clean(stages):
+    # hc_post of the previous sublayer in front: the square warps rewrite
+    # each stage in place and the MMA waits for all four of them
+    for seed in range(40):
+        simulate(ctas=4, tiles=8, stages_per_tile=stages, slots=3, lag=3, bufs=4, post=True,
+                 seed=seed)
+
+
+def test_mma_waiting_for_the_load_instead_of_the_rewrite_is_caught():
+    assert _fails(ctas=4, tiles=6, stages_per_tile=2, slots=3, lag=3, bufs=4, post=True,
+                  mutation="mma_waits_full")
+
+
 def test_full_cluster_of_sixteen():
     for seed in range(3):
         simulate(ctas=16, tiles=4, stages_per_tile=5, slots=3, lag=3, bufs=4, seed=seed)
