@@ -57,6 +57,11 @@ __device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
 __device__ __forceinline__ void ffma2(uint64_t &d, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
 }
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ float sum2(uint64_t v) {
     float lo, hi;
     unpack2(v, lo, hi);

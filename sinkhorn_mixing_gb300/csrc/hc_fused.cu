@@ -74,19 +74,46 @@ constexpr int kLag = 3;
 constexpr int kColDoneBufs = 4;  // > kLag: the awaited phase is unambiguous
 static_assert(kColDoneBufs > kLag, "pre staging and col_done must outlive the lag");
 
-// warp roles (16 warps: 512 threads leave 128 registers per thread)
+// warp roles.  hc_mixes_pre: 16 warps (512 threads, 128 registers each);
+// with POST (hc_post in front) 20 warps (96 registers: 5 warps per SM
+// sub-partition), 8 of them computing the new stream.
 constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpSq0 = 2;      // 2..5: sums of squares, 16 tokens each
+constexpr int kWarpMma = 1;      // lane 0 issues the MMAs (and with POST the x_next stores)
 constexpr int kWarpEpi0 = 8;     // 8, 9: TMEM read-out (lanes 0..63), records to owners
 constexpr int kWarpOwner = 12;   // reduces the records of this CTA's tokens, Sinkhorn
-constexpr int kCollapseWarps = 7;  // 6, 7, 10, 11, 13, 14, 15
-constexpr int kThreads = 16 * 32;
+constexpr int kCollapseWarps = 7;
 constexpr int kCollapseThreads = kCollapseWarps * 32;
-
-__host__ __device__ constexpr int collapse_index(int warp) {
-    return warp == 6 ? 0 : warp == 7 ? 1 : warp == 10 ? 2 : warp == 11 ? 3 : warp - 9;
-}
+template <bool POST>
+struct Roles {
+    static constexpr int kWarps = POST ? 20 : 16;
+    static constexpr int kThreads = kWarps * 32;
+    // square warps (with POST: post warps): 2..5, or 2..7, 10, 11
+    static constexpr int kSqWarps = POST ? 8 : 4;
+    __host__ __device__ static constexpr int sq_index(int w) {
+        return (w >= 2 && w < (POST ? 8 : 6)) ? w - 2 : (POST && (w == 10 || w == 11)) ? w - 4 : -1;
+    }
+    // collapse warps: 6, 7, 10, 11, 13, 14, 15, or 13..19
+    __host__ __device__ static constexpr int col_index(int w) {
+        return POST ? (w >= 13 && w < 20 ? w - 13 : -1)
+                    : (w == 6 ? 0 : w == 7 ? 1 : w == 10 ? 2 : w == 11 ? 3
+                                                 : (w >= 13 && w < 16 ? w - 9 : -1));
+    }
+    // Ring consumers: the MMA commit and the square warps; with POST the MMA
+    // commit and the MMA thread once the slot's TMA store has read it (the
+    // post warps are done with a slot when they arrive on post_done, before
+    // either of those reads it).
+    static constexpr int kEmptyArrivals = POST ? 2 : 1 + kSqWarps;
+    // sq_full: the square warps, and with POST the MMA thread once the
+    // tile's new stream is written and visible (the epilogue waits for it
+    // before the tile's records go out, and so before any collapse re-reads)
+    static constexpr int kSqFullArrivals = kSqWarps + (POST ? 1 : 0);
+    // lanes per token row in the square warps: a lane covers 8 / kLanesPerRow
+    // 16-byte pieces (8 channels each) of each copy
+    static constexpr int kLanesPerRow = POST ? 4 : 2;
+    static constexpr int kPieces = 8 / kLanesPerRow;
+};
+constexpr int kThreadsPlain = Roles<false>::kThreads;
+constexpr int kThreadsPost = Roles<true>::kThreads;
 
 // tcgen05 instruction descriptor: D f32, A/B bf16, both K-major, N=48, M=128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNW >> 3) << 17) |
@@ -130,6 +157,35 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// TMA store of a [64 x 64] x 4 box from shared memory, and the bulk-group
+// bookkeeping that tells when it has read the slot / written memory.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                             int c3, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// L2 prefetch of a [64 x 64] box of a 2-D tensor
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- layout
 
 struct Smem {
@@ -157,8 +213,6 @@ __host__ __device__ constexpr int bColDone(int i) { return 2 * kSlots + 10 + kCo
 constexpr int kMmaDrain = 2 * kSlots + 10 + 2 * kColDoneBufs;
 __host__ __device__ constexpr int bPostDone(int s) { return kMmaDrain + 1 + s; }
 constexpr int kNumBars = kMmaDrain + 1 + kSlots;
-// Ring consumers: the MMA thread (through tcgen05.commit) and the 4 square warps.
-constexpr int kEmptyArrivals = 5;
 
 constexpr size_t kRingBytes = (size_t)kSlots * kStageBytes;
 constexpr size_t kRecvBytes = (size_t)kCluster * kOwn * kRec * 4;
@@ -204,8 +258,11 @@ __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams
 // NCC = w / 64 (64-channel sub-tiles per copy per CTA) is a template
 // parameter so that all index arithmetic is by constants.
 template <int NCC, bool POST>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_fused(const __grid_constant__ CUtensorMap tmap, const FusedParams p) {
+__global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
+    k_fused(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_xn,
+            const __grid_constant__ CUtensorMap tmap_out, const FusedParams p) {
+    using R = Roles<POST>;
+    constexpr int kThreads = R::kThreads;
     extern __shared__ uint8_t smem_raw[];
     constexpr int ncc = NCC;
     const Smem sm = carve(smem_raw, ncc);
@@ -223,12 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort = 0;
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(bFull(s)), 1);
-            mbar_init(bar(bEmpty(s)), kEmptyArrivals);
+            mbar_init(bar(bEmpty(s)), R::kEmptyArrivals);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(bAccFull(b)), 1);
             mbar_init(bar(bAccEmpty(b)), 2);
-            mbar_init(bar(bSqFull(b)), 4);
+            mbar_init(bar(bSqFull(b)), R::kSqFullArrivals);
             mbar_init(bar(bSqEmpty(b)), 2);
         }
         mbar_init(bar(kRecvFull), 1);
@@ -238,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(bColDone(i)), kCollapseWarps);
         }
         mbar_init(bar(kMmaDrain), 1);
-        for (int s = 0; s < kSlots; ++s) mbar_init(bar(bPostDone(s)), 4);
+        for (int s = 0; s < kSlots; ++s) mbar_init(bar(bPostDone(s)), R::kSqWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_expect_tx(bar(kRecvFull), kRecvTx);
         // The first stages' loads go out now, so that their latency overlaps
@@ -250,6 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(su32(sm.ring + q * kStageBytes), &tmap, 0, (cluster + (q / ncc) * nclusters) * kTM,
                         (q % ncc) * kCluster + rank, 0, bar(bFull(q)));
         }
+        // POST: the first tile's sublayer output into L2 (the post warps
+        // read it with plain loads, one stage ahead)
+        if (POST && T > 0)
+            for (int cc = 0; cc < ncc; ++cc)
+                tma_prefetch_2d(&tmap_out, (cc * kCluster + rank) * 64, cluster * kTM);
     }
     if (warp == kWarpMma) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -263,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // piece of W is read once for both rows, with kPieces pieces in flight
     // per thread (one piece at a time waited a full L2 round trip each).
     {
-        constexpr int kPieces = 8;
+        constexpr int kPieces = POST ? 4 : 8;  // 96 registers with POST
         const int nkc = 4 * ncc;
         const int total = kMix * nkc * 8;  // (piece q, row i, chunk kc)
         const int64_t F = 4LL * p.d;
@@ -338,6 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          (uint32_t)(tw / kColDoneBufs) & 1, abort, p.err))
                         break;
                 }
+                // POST: the next tile's sublayer output into L2, a tile ahead
+                if (POST && it + 1 < T)
+                    for (int cc = 0; cc < ncc; ++cc)
+                        tma_prefetch_2d(&tmap_out, (cc * kCluster + rank) * 64, (tile + nclusters) * kTM);
                 for (int cc = 0; cc < ncc; ++cc) {
                     const uint32_t q = (uint32_t)(ncc * it + cc);
                     const int slot = (int)(q % kSlots);
@@ -367,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0; it < T && ok; ++it) {
                 const int b = it & 1;
                 const uint32_t use = (uint32_t)(it >> 1);
-                if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) break;
+                if (!wait_bar<false>(bar(bAccEmpty(b)), (use & 1) ^ 1, abort, p.err)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + (uint32_t)(b * 64);
                 for (int cc = 0; cc < ncc; ++cc) {
@@ -392,37 +461,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      (cc | j | k) != 0);
                     }
                     mma_commit(bar(bEmpty(slot)));
+                    if (POST) {
+                        // x_next: the rewritten stage goes out by one TMA
+                        // store straight from its slot (rows past n are
+                        // clipped by the tensor map).  A slot is released once
+                        // its store has read it.
+                        tma_store_4d(&tmap_xn, 0, (cluster + it * nclusters) * kTM,
+                                     cc * kCluster + rank, 0, a0);
+                        bulk_commit();
+                        if (cc + 1 < ncc) {
+                            bulk_wait_read<0>();
+                        } else {
+                            // The tile's stores are complete and visible
+                            // GPU-wide before its sq_full arrival, which the
+                            // epilogue awaits before the tile's records leave
+                            // for the owners (whose collapse re-reads x_next).
+                            bulk_wait<0>();
+                            asm volatile("fence.proxy.async.global;" ::: "memory");
+                            __threadfence();
+                            mbar_arrive(bar(bSqFull(b)));
+                        }
+                        mbar_arrive(bar(bEmpty(slot)));
+                    }
                 }
                 if (!ok) break;
                 mma_commit(bar(bAccFull(b)));
             }
+            // nothing may still read this CTA's shared memory at exit
+            if (POST) bulk_wait<0>();
             // all issued MMAs complete before TMEM is freed
             mma_commit(bar(kMmaDrain));
             wait_bar<false>(bar(kMmaDrain), 0, abort, p.err);
         }
-    } else if (warp >= kWarpSq0 && warp < kWarpSq0 + 4) {
-        // Sums of squares: warp 2+g covers tokens 16g..16g+15 of every stage;
-        // lane -> token 16g + lane/2, half lane%2 of each 128-byte row.  With
-        // POST these warps also compute the new stream (hc_post) first.
-        const int i = 16 * (warp - kWarpSq0) + (lane >> 1);
-        const int h = lane & 1;
+    } else if (R::sq_index(warp) >= 0) {
+        // Sums of squares of every stage: token i of the tile, lanes
+        // kLanesPerRow per 128-byte row, kPieces 16-byte pieces each.  With
+        // POST these warps first compute the new stream (hc_post) in place.
+        constexpr int LP = R::kLanesPerRow, PP = R::kPieces;
+        const int i = (32 / LP) * R::sq_index(warp) + lane / LP;
+        const int part = lane % LP;  // pieces PP*part .. PP*part + PP-1 of each row
         auto tile_of = [&](uint32_t q) { return cluster + (int)(q / ncc) * nclusters; };
-        // POST: the sublayer output's 32 channels of this thread's row for
+        // POST: the sublayer output's 8*PP channels of this thread's row for
         // stage q, loaded one stage ahead; the token's post and comb per tile
-        uint4 onext[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                          make_uint4(0, 0, 0, 0)};
+        uint4 onext[PP];
+#pragma unroll
+        for (int m = 0; m < PP; ++m) onext[m] = make_uint4(0, 0, 0, 0);
         auto prefetch_out = [&](uint32_t q) {
             if (!POST || q >= (uint32_t)(ncc * T)) return;
             const int64_t tok = (int64_t)tile_of(q) * kTM + i;
             if (tok >= p.n) {
 #pragma unroll
-                for (int m = 0; m < 4; ++m) onext[m] = make_uint4(0, 0, 0, 0);
+                for (int m = 0; m < PP; ++m) onext[m] = make_uint4(0, 0, 0, 0);
                 return;
             }
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.out + tok * (int64_t)p.d + (int)(q % ncc) * (kCluster * 64) + rank * 64 + 32 * h);
+                p.out + tok * (int64_t)p.d + (int)(q % ncc) * (kCluster * 64) + rank * 64 +
+                8 * PP * part);
 #pragma unroll
-            for (int m = 0; m < 4; ++m) onext[m] = ld_stream(src + m);
+            for (int m = 0; m < PP; ++m) onext[m] = ld_stream(src + m);
         };
         float po[4] = {0.f, 0.f, 0.f, 0.f}, cmf[4][4];  // the token's post and comb
         prefetch_out(0);
@@ -430,7 +526,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0; it < T && ok; ++it) {
             const int b = it & 1;
             const uint32_t use = (uint32_t)(it >> 1);
-            uint64_t s2[4] = {0, 0, 0, 0};  // independent packed sums: short FMA chains
+            // One packed accumulator set per 32-channel quarter of the row
+            // (pieces 2a, 2a+1), summed in the order (stage, piece, copy) and
+            // then as ((q0 + q1) + (q2 + q3)): the same sums whichever lanes
+            // hold the quarters, so both variants agree bit for bit.
+            uint64_t s2[PP / 2][4];
+#pragma unroll
+            for (int a2 = 0; a2 < PP / 2; ++a2)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s2[a2][e] = 0;
             if (POST) {
                 const int64_t tok = (int64_t)tile_of((uint32_t)(ncc * it)) * kTM + i;
                 float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), cv[4];
@@ -456,16 +560,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const uint32_t base = su32(sm.ring + slot * kStageBytes) + i * 128;
-                // 16-byte piece m (8 channels) of copy j of this thread's row,
-                // 128-byte swizzle: 8 consecutive lanes hit 8 bank groups
+                // 16-byte piece m of copy j of this thread's row, 128-byte
+                // swizzle: the lanes of one quarter-warp hit distinct bank groups
                 auto piece = [&](int j, int m) -> uint32_t {
-                    return base + j * kSubBytes + (((4 * h + m) ^ (i & 7)) << 4);
+                    return base + j * kSubBytes + (((PP * part + m) ^ (i & 7)) << 4);
                 };
-                // squares in the order (piece, copy): the same order in both
-                // variants, so that they give the same sums
                 if (!POST) {
 #pragma unroll
-                    for (int m = 0; m < 4; ++m)
+                    for (int m = 0; m < PP; ++m)
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint4 v = lds128(piece(j, m));
@@ -473,23 +575,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
                                 const uint64_t xp = bf16x2_to_f32x2(wv[e]);
-                                ffma2(s2[e], xp, xp);
+                                ffma2(s2[m / 2][e], xp, xp);
                             }
                         }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
                 } else {
                     // hc_post ("Mix projection" page, Block.hc_post) of this
-                    // thread's 32 channels of the stage, one 8-channel piece
-                    // at a time: x'_k = post_k out + sum_j comb[j][k] x_j, the
+                    // thread's channels of the stage, one 8-channel piece at a
+                    // time: x'_k = post_k out + sum_j comb[j][k] x_j, the
                     // product first, then the copies j = 0..3 in order (as
                     // hc_post); written back over the residual in the slot
                     // (all four input copies of a piece are read before any is
-                    // written) and to x_next.
-                    const uint4 ocur[4] = {onext[0], onext[1], onext[2], onext[3]};
-                    prefetch_out(q + 1);
-                    const int64_t tok = (int64_t)tile_of(q) * kTM + i;
-                    const int ch0 = cc * (kCluster * 64) + rank * 64 + 32 * h;
+                    // written).  The store thread writes the slot to x_next.
+                    uint4 ocur[PP];
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
+                    for (int m = 0; m < PP; ++m) ocur[m] = onext[m];
+                    prefetch_out(q + 1);
+#pragma unroll
+                    for (int m = 0; m < PP; ++m) {
                         // the piece's inputs as packed binary32 pairs, once
                         uint64_t xp[4][4], op[4];
 #pragma unroll
@@ -509,10 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint64_t acc2[4];
                             const uint64_t pk = pack2(po[k], po[k]);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                acc2[e] = 0x8000000080000000ull;  // -0: the product alone
-                                ffma2(acc2[e], pk, op[e]);
-                            }
+                            for (int e = 0; e < 4; ++e) acc2[e] = fmul2(pk, op[e]);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint64_t cmk = pack2(cmf[j][k], cmf[j][k]);
@@ -526,34 +627,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 unpack2(acc2[e], lo, hi);
                                 nw[e] = pack_bf16x2(lo, hi);
                                 const uint64_t xq = bf16x2_to_f32x2(nw[e]);
-                                ffma2(s2[e], xq, xq);
+                                ffma2(s2[m / 2][e], xq, xq);
                             }
-                            const uint4 nv = make_uint4(nw[0], nw[1], nw[2], nw[3]);
-                            sts128(piece(k, m), nv);
-                            if (tok < p.n)
-                                st_stream(reinterpret_cast<uint4 *>(
-                                              p.x_next + (tok * 4 + k) * (int64_t)p.d + ch0 + 8 * m),
-                                          nv);
+                            sts128(piece(k, m), make_uint4(nw[0], nw[1], nw[2], nw[3]));
                         }
                     }
-                    // the new stream in the slot, for the tensor core (async proxy)
+                    // the new stream in the slot, for the tensor core and the
+                    // TMA store (async proxy)
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(bPostDone(slot)));
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
             }
             if (!ok) break;
-            // POST: the tile's x_next is visible GPU-wide before its records
-            // (and so before any owner's collapse re-reads it)
-            if (POST) __threadfence();
-            float ss = (sum2(s2[0]) + sum2(s2[1])) + (sum2(s2[2]) + sum2(s2[3]));
-            ss += __shfl_xor_sync(0xFFFFFFFFu, ss, 1);
+            float ss = 0.f;
+#pragma unroll
+            for (int a2 = 0; a2 < PP / 2; ++a2) {
+                const float qs = (sum2(s2[a2][0]) + sum2(s2[a2][1])) +
+                                 (sum2(s2[a2][2]) + sum2(s2[a2][3]));
+                ss = a2 == 0 ? qs : ss + qs;
+            }
+#pragma unroll
+            for (int sh = 1; sh < LP; sh <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, sh);
             if (!__all_sync(0xFFFFFFFFu,
                             wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
                 break;
-            if (h == 0) sm.sq[b * kTM + i] = ss;
+            if (part == 0) sm.sq[b * kTM + i] = ss;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bSqFull(b)));
         }
@@ -692,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile, over all d channels: 7 warps, 224 threads.  Output vector
         // o = (token u = o / nv, 8 channels at 8*(o % nv)); 4 vectors in flight
         // per thread, each needing the 4 copies (16-byte loads from L2).
-        const int ct = collapse_index(warp) * 32 + lane;
+        const int ct = R::col_index(warp) * 32 + lane;
         constexpr int nv = NCC * 8 * kCluster;  // vectors per copy row (d / 8)
         constexpr int nout = kOwn * nv;
         const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
@@ -704,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                          p.err)))
                 break;
             const int64_t tok0 = (int64_t)tile * kTM + rank * kOwn;
-            constexpr int G = 4;
+            constexpr int G = POST ? 3 : 4;  // 96 registers with POST
             for (int o0 = ct; o0 < nout; o0 += G * kCollapseThreads) {
                 uint4 xv[G][4];
 #pragma unroll
@@ -766,12 +865,12 @@ struct DevState {
     bool init = false;
     unsigned long long ctx = 0;  // the context the set-up below was done in
     bool ok = false;
-    int max_clusters = 0;
+    int max_clusters[2] = {0, 0};  // co-resident clusters, without / with POST
 };
 std::mutex g_fmu;
 DevState g_dev[64];
 
-using FusedKernel = void (*)(CUtensorMap, FusedParams);
+using FusedKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
 
 // The instantiation for w = 64 * ncc channels per CTA (POST: with the
 // previous sublayer's hc_post in front).
@@ -805,25 +904,26 @@ const DevState &dev_state(const DeviceInfo &di) {
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
                 return st;
         }
-    const size_t smem = smem_bytes(kMaxNcc);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = kCluster;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int nc = 0;
-    if (cudaOccupancyMaxActiveClusters(&nc, kernel_for(kMaxNcc, true), &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return st;
+    for (int post = 0; post < 2; ++post) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kCluster);
+        cfg.blockDim = dim3(post ? kThreadsPost : kThreadsPlain);
+        cfg.dynamicSmemBytes = smem_bytes(kMaxNcc);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = kCluster;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kernel_for(kMaxNcc, post), &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return st;
+        }
+        st.max_clusters[post] = nc;
     }
-    st.max_clusters = nc;
-    st.ok = nc > 0;
+    st.ok = st.max_clusters[0] > 0 && st.max_clusters[1] > 0;
     return st;
 }
 
@@ -866,6 +966,26 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // with POST the same view of x_next, for the stores of the rewritten
+    // stages, and a 2-D view {channel, token} of the sublayer output, for
+    // its L2 prefetches
+    CUtensorMap tmap_xn = tmap, tmap_out = tmap;
+    if (with_post) {
+        r = tensor_map_encoder()(&tmap_xn, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, x_next, gdim,
+                                 gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint64_t odim[2] = {(cuuint64_t)d, (cuuint64_t)n};
+        const cuuint64_t ostride[1] = {(cuuint64_t)(d * 2)};
+        const cuuint32_t obox[2] = {64, kTM};
+        r = tensor_map_encoder()(&tmap_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                                 const_cast<uint16_t *>(out), odim, ostride, obox, estride,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
     FusedParams p;
     p.n = n;
     p.d = (int)d;
@@ -890,10 +1010,11 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
     p.post_in = post_in;
     p.comb_in = comb_in;
     p.x_next = x_next;
-    const int nclusters = p.num_tiles < st.max_clusters ? p.num_tiles : st.max_clusters;
+    const int mc = st.max_clusters[with_post ? 1 : 0];
+    const int nclusters = p.num_tiles < mc ? p.num_tiles : mc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(with_post ? kThreadsPost : kThreadsPlain);
     cfg.dynamicSmemBytes = smem_bytes(p.ncc);
     cfg.stream = s;
     cudaLaunchAttribute attr;
@@ -903,7 +1024,7 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc, with_post), tmap, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc, with_post), tmap, tmap_xn, tmap_out, p);
     if (e != cudaSuccess) return e;
     return launched();
 }

@@ -10,18 +10,26 @@ the kernel's roles as generators that yield the barrier waits they make:
             its full barrier and issues a load that lands later;
   mma       per tile, waits for a free accumulator, consumes every stage in
             order and releases each slot by a commit (commits complete in
-            issue order), then commits acc_full;
+            issue order), then commits acc_full; with `post` it waits for
+            post_done instead of full, and also stores each rewritten stage
+            from its slot by a bulk copy that reads the slot later and writes
+            memory later still: it waits until that store has read the slot
+            and releases it, and at a tile's last stage waits until the
+            tile's stores are written and arrives on its sq_full first;
   sq (x4)   consume every stage in order, release it, publish the tile's sums
-            of squares through sq_full / sq_empty; with `post` they first
-            rewrite the stage in place (hc_post of the previous sublayer) and
-            signal post_done, which the MMA waits for instead of full;
+            of squares through sq_full / sq_empty; with `post` (x8) they
+            first rewrite the stage in place (hc_post of the previous
+            sublayer) and signal post_done, and leave the release to the MMA
+            thread;
   epi (x2)  read the accumulator and the squares, wait until the previous
             tile's records were read (recv_free), then send their records to
             the owners, whose recv_full they complete by bytes;
   owner     waits for its records, reads them, stages pre and signals
             pre_ready, re-arms recv_full, then releases the record buffer to
             every sender;
-  collapse  (x2) waits for pre, reads the staging slot, signals col_done.
+  collapse  (x2) waits for pre, reads the staging slot (with `post`, and
+            the tile's new stream as every CTA of the cluster stored it),
+            signals col_done.
 
 Up to three randomly chosen roles run a hundred times slower than the rest,
 so that single slow roles fall far behind and early-reuse windows are
@@ -77,6 +85,21 @@ def wait(bar, parity):
     return ("wait", bar, parity)
 
 
+class Cond:
+    """A wait on a condition that the hardware guarantees to become true
+    (completion of bulk copies already issued)."""
+
+    def __init__(self, fn):
+        self.fn = fn
+
+    def try_wait(self, _parity):
+        return self.fn()
+
+
+def until(fn):
+    return ("wait", Cond(fn), None)
+
+
 STEP = ("step",)
 
 
@@ -84,8 +107,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
              seed=0, mutation=None, post=False):
     """Run one random interleaving; raises ProtocolError on any violation.
     `mutation` plants a known protocol mistake (for the tests that show the
-    model can fail): "release_before_read", "empty_parity", "mma_waits_full"
-    (with post)."""
+    model can fail): "release_before_read", "empty_parity", and with post
+    "mma_waits_full", "release_before_store_read", "visible_before_written"."""
     rnd = random.Random(seed)
     events = []
 
@@ -93,20 +116,24 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
         events.append(fn)
 
     C, T, NS, S = ctas, tiles, stages_per_tile, slots
+    NSQ = 8 if post else 4
+    written = set()  # (rank, stage) of x_next stores that reached memory
     cs = []
     for r in range(C):
         cs.append(dict(
             full=[Barrier("full", 1) for _ in range(S)],
-            post_done=[Barrier("post_done", 4) for _ in range(S)],
+            post_done=[Barrier("post_done", NSQ) for _ in range(S)],
             posted=[set() for _ in range(S)],
-            empty=[Barrier("empty", 5) for _ in range(S)],  # MMA commit + 4 square warps
+            # MMA commit + 4 square warps; with post MMA commit + store read
+            empty=[Barrier("empty", 2 if post else 5) for _ in range(S)],
+            stores=[],
             slot=[None] * S, holders=[set() for _ in range(S)],
             acc_full=[Barrier("acc_full", 1) for _ in range(2)],
             acc_empty=[Barrier("acc_empty", 2) for _ in range(2)],
             acc=[None, None], acc_readers=[0, 0],
-            sq_full=[Barrier("sq_full", 4) for _ in range(2)],
+            sq_full=[Barrier("sq_full", NSQ + (1 if post else 0)) for _ in range(2)],
             sq_empty=[Barrier("sq_empty", 2) for _ in range(2)],
-            sq=[[None] * 4, [None] * 4],
+            sq=[[None] * NSQ, [None] * NSQ],
             recv_full=Barrier("recv_full", 1), recv_free=Barrier("recv_free", C),
             recv=[None] * C, reading=[False],
             pre_ready=[Barrier("pre_ready", 1) for _ in range(bufs)],
@@ -135,8 +162,27 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                     c["full"][s].complete_tx(1)
                 later(land)
 
-    def mma(c):
+    def mma(c, rank):
         chain = []
+        stores = c["stores"]
+
+        def store(s, q):
+            rec = dict(q=q, read=False, written=False)
+            stores.append(rec)
+            c["holders"][s].add(("store", q))
+
+            def read(rec=rec, s=s, q=q):
+                rec["read"] = True
+                c["holders"][s].discard(("store", q))
+
+                def write(rec=rec, q=q):
+                    rec["written"] = True
+                    written.add((rank, q))
+                later(write)
+            later(read)
+
+        def all_done(key):
+            return lambda: all(r[key] for r in stores)
 
         def commit():
             kind, a, b = chain.pop(0)
@@ -158,11 +204,23 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                 yield wait(c["post_done" if waits_post else "full"][s], (q // S) & 1)
                 if c["slot"][s] != q:
                     raise ProtocolError("MMA wants stage %d, slot holds %s" % (q, c["slot"][s]))
-                if post and len(c["posted"][s]) != 4:
+                if post and len(c["posted"][s]) != NSQ:
                     raise ProtocolError("MMA reads stage %d before it was rewritten" % q)
                 c["holders"][s].add("mma")
                 chain.append(("empty", s, None))
                 later(commit)
+                if post:
+                    store(s, q)
+                    if st + 1 < NS:
+                        if mutation != "release_before_store_read":
+                            yield until(all_done("read"))
+                    else:
+                        if mutation != "visible_before_written":
+                            yield until(all_done("written"))
+                        elif mutation != "release_before_store_read":
+                            yield until(all_done("read"))
+                        c["sq_full"][b].arrive()
+                    c["empty"][s].arrive()
             chain.append(("acc", b, it))
             later(commit)
 
@@ -179,9 +237,11 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                 yield STEP
                 if post:
                     c["posted"][s].add(w)
+                    c["holders"][s].discard(w)
                     c["post_done"][s].arrive()
-                c["holders"][s].discard(w)
-                c["empty"][s].arrive()
+                else:
+                    c["holders"][s].discard(w)
+                    c["empty"][s].arrive()
             yield wait(c["sq_empty"][b], ((it >> 1) & 1) ^ 1)
             c["sq"][b][w] = it
             c["sq_full"][b].arrive()
@@ -198,8 +258,11 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             c["acc_readers"][b] -= 1
             c["acc_empty"][b].arrive()
             yield wait(c["sq_full"][b], (it >> 1) & 1)
-            if c["sq"][b] != [it] * 4:
+            if c["sq"][b] != [it] * NSQ:
                 raise ProtocolError("read-out finds squares %s" % c["sq"][b])
+            if post and any((rank, NS * it + st) not in written for st in range(NS)):
+                raise ProtocolError("records of tile %d leave before its new stream is written"
+                                    % it)
             c["sq_empty"][b].arrive()
             yield wait(c["recv_free"], (it & 1) ^ 1)
             for o in mine:
@@ -242,6 +305,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             yield wait(c["pre_ready"][i], (it // bufs) & 1)
             if c["stage"][i] != it:
                 raise ProtocolError("collapse of tile %d reads the pre of %s" % (it, c["stage"][i]))
+            if post and any((r, NS * it + st) not in written for r in range(C) for st in range(NS)):
+                raise ProtocolError("collapse of tile %d re-reads a stream not yet written" % it)
             c["stage_readers"][i] += 1
             yield STEP
             c["stage_readers"][i] -= 1
@@ -249,7 +314,7 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
 
     roles = []
     for r, c in enumerate(cs):
-        roles += [producer(c), mma(c), owner(c)] + [sq(c, w) for w in range(4)]
+        roles += [producer(c), mma(c, r), owner(c)] + [sq(c, w) for w in range(NSQ)]
         roles += [epi(c, r, h) for h in range(2)]
         if not mixes_only:
             roles += [collapse(c), collapse(c)]

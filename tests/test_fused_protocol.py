@@ -19,8 +19,9 @@ def test_kernel_configuration_runs_clean(stages, mixes_only):
 
 @pytest.mark.parametrize("stages", [1, 3, 5])
 def test_post_variant_runs_clean(stages):
-    # hc_post of the previous sublayer in front: the square warps rewrite
-    # each stage in place and the MMA waits for all four of them
+    # hc_post of the previous sublayer in front: 8 warps rewrite each stage
+    # in place, the MMA waits for all of them, and the MMA thread stores the
+    # rewritten stage and releases the slot and the tile's records
     for seed in range(40):
         simulate(ctas=4, tiles=8, stages_per_tile=stages, slots=3, lag=3, bufs=4, post=True,
                  seed=seed)
@@ -29,6 +30,17 @@ def test_post_variant_runs_clean(stages):
 def test_mma_waiting_for_the_load_instead_of_the_rewrite_is_caught():
     assert _fails(ctas=4, tiles=6, stages_per_tile=2, slots=3, lag=3, bufs=4, post=True,
                   mutation="mma_waits_full")
+
+
+def test_releasing_a_slot_before_its_store_read_it_is_caught():
+    assert _fails(ctas=4, tiles=6, stages_per_tile=2, slots=3, lag=3, bufs=4, post=True,
+                  mutation="release_before_store_read")
+
+
+@pytest.mark.parametrize("stages", [1, 3])
+def test_records_before_the_new_stream_is_written_are_caught(stages):
+    assert _fails(ctas=4, tiles=6, stages_per_tile=stages, slots=3, lag=3, bufs=4, post=True,
+                  mutation="visible_before_written")
 
 
 def test_full_cluster_of_sixteen():
