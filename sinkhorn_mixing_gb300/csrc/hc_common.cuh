@@ -110,10 +110,27 @@ __device__ __forceinline__ void split_pre_post(MixFn m, BaseFn base, float s0, f
     for (int j = 0; j < HC; ++j) post[j] = 2.0f * sigmoidf_(fmaf(m(HC + j), s1, base(HC + j)));
 }
 
+// Pairwise sum of v[0..N) (N a power of two): ((v0 + v1) + (v2 + v3)) + ...
+// A shorter dependency chain than the sum in index order, which the
+// Sinkhorn steps below are bound by.
+template <int N>
+__device__ __forceinline__ float pair_sum(const float (&v)[N]) {
+    static_assert((N & (N - 1)) == 0, "a power of two");
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = v[i];
+#pragma unroll
+    for (int h = N / 2; h >= 1; h /= 2)
+#pragma unroll
+        for (int i = 0; i < h; ++i) t[i] = t[2 * i] + t[2 * i + 1];
+    return t[0];
+}
+
 // comb of one token (same kernel on the same page): with
 //   L_jk = m_{2HC+j HC+k} s2 + b_{2HC+j HC+k}   (row j, column k)
 // C = row softmax of L (max-subtracted, plain row sum) + eps; a column step;
 // then (iters-1) x (row step, column step), each step dividing by (sum + eps).
+// Rows and columns are summed pairwise (pair_sum).
 template <int HC, typename MixFn, typename BaseFn>
 __device__ __forceinline__ void sinkhorn_comb(MixFn m, BaseFn base, float s2, int iters, float eps,
                                               float C[HC][HC]) {
@@ -127,45 +144,36 @@ __device__ __forceinline__ void sinkhorn_comb(MixFn m, BaseFn base, float s2, in
         float mx = C[j][0];
 #pragma unroll
         for (int k = 1; k < HC; ++k) mx = fmaxf(mx, C[j][k]);
-        float s = 0.0f;
+        float e[HC];
 #pragma unroll
-        for (int k = 0; k < HC; ++k) {
-            C[j][k] = expf(C[j][k] - mx);
-            s += C[j][k];
-        }
-        const float inv = rcp_refined(s);  // s >= 1: the row maximum contributes e^0
+        for (int k = 0; k < HC; ++k) e[k] = C[j][k] = expf(C[j][k] - mx);
+        const float inv = rcp_refined(pair_sum(e));  // >= 1: the row maximum contributes e^0
 #pragma unroll
         for (int k = 0; k < HC; ++k) C[j][k] = fmaf(C[j][k], inv, eps);
     }
-    // column step
+    auto row_step = [&]() {
 #pragma unroll
-    for (int k = 0; k < HC; ++k) {
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < HC; ++j) s += C[j][k];
-        const float inv = rcp_refined(s + eps);
-#pragma unroll
-        for (int j = 0; j < HC; ++j) C[j][k] *= inv;
-    }
-    for (int it = 1; it < iters; ++it) {
-#pragma unroll
-        for (int j = 0; j < HC; ++j) {  // row step
-            float s = 0.0f;
-#pragma unroll
-            for (int k = 0; k < HC; ++k) s += C[j][k];
-            const float inv = rcp_refined(s + eps);
+        for (int j = 0; j < HC; ++j) {
+            const float inv = rcp_refined(pair_sum(C[j]) + eps);
 #pragma unroll
             for (int k = 0; k < HC; ++k) C[j][k] *= inv;
         }
+    };
+    auto col_step = [&]() {
 #pragma unroll
-        for (int k = 0; k < HC; ++k) {  // column step
-            float s = 0.0f;
+        for (int k = 0; k < HC; ++k) {
+            float c[HC];
 #pragma unroll
-            for (int j = 0; j < HC; ++j) s += C[j][k];
-            const float inv = rcp_refined(s + eps);
+            for (int j = 0; j < HC; ++j) c[j] = C[j][k];
+            const float inv = rcp_refined(pair_sum(c) + eps);
 #pragma unroll
             for (int j = 0; j < HC; ++j) C[j][k] *= inv;
         }
+    };
+    col_step();
+    for (int it = 1; it < iters; ++it) {
+        row_step();
+        col_step();
     }
 }
 
