@@ -10,9 +10,8 @@
 //   * CTA r of a cluster owns channels [r*w, (r+1)*w) of every copy
 //     (w = d/16) and keeps its slice of W_mix (fp32, 24 x 4 x w) and of its
 //     tokens' x (bf16, tokens x 4 x w) in shared memory.
-//   * The slices arrive by bulk asynchronous copies (one per row of a copy j),
-//     one barrier per copy j; the projection of copy j starts when its
-//     barrier completes.
+//   * The slices arrive by asynchronous copies, one group per copy j; the
+//     projection of copy j starts when its group is in.
 //   * Partial mix numbers and sums of squares on CUDA cores (packed
 //     two-wide fma): warp (g, h) takes tokens 4g..4g+3 and mixes 6h..6h+5
 //     over all 4w features, each lane the feature pairs 64 apart starting at
@@ -23,7 +22,7 @@
 //     with asynchronous 4-byte stores whose bytes complete the owner's
 //     barrier.  The owner sums the 16 records in CTA order, forms r, m and
 //     pre, sends pre to all 16 CTAs the same way and then runs the Sinkhorn
-//     for comb.
+//     for comb on 16 lanes, one comb entry each.
 //   * Every CTA collapses its own w channels of the cluster's tokens from the
 //     x slice it holds, so x is read from memory once.
 //
@@ -81,22 +80,20 @@ struct DecodeParams {
 
 __host__ __device__ constexpr int round4(int t) { return (t + 3) & ~3; }
 
-// Bulk asynchronous copy global -> this CTA's shared memory of `bytes`
-// (a multiple of 16, both addresses 16-byte aligned); its bytes complete
-// the transaction count of `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
+// 16-byte asynchronous copy global -> shared (cached in L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// Bounded wait that ignores the abort flag: at exit, for this CTA's own
-// copies still in flight after an abort.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = gtimer();
-    while (!mbar_try(bar, parity) && gtimer() - t0 < kTimeoutNs) {
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most `left` of this thread's copy groups are still pending.
+__device__ __forceinline__ void cp_async_wait(int left) {
+    switch (left) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
     }
 }
 
@@ -112,7 +109,7 @@ __host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
 }
 __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
     return wreg_bytes(w) + xreg_bytes(w, tpc) + kCluster * kRecStride * 4 + kMaxTok * 4 * 4 +
-           kCluster * kMaxTok * 4 + 7 * 8 + 16;
+           kCluster * kMaxTok * 4 + 3 * 8 + 16;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
@@ -126,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     float *preb = recv + kCluster * kRecStride;     // [16][4]: pre of the cluster's tokens
     float *normp = preb + kMaxTok * 4;              // [16 senders][16 tokens]: partial sums of y^2
     uint64_t *bars = reinterpret_cast<uint64_t *>(normp + kCluster * kMaxTok);
-    int *abort_word = reinterpret_cast<int *>(bars + 7);
+    int *abort_word = reinterpret_cast<int *>(bars + 3);
     volatile int *abort = abort_word;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
@@ -134,55 +131,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     const int tv = (int)((int64_t)p.n - tok0 < p.tpc ? (int64_t)p.n - tok0 : p.tpc);
     const bool mixes_only = p.mixes_only != 0;
     const uint32_t bRecv = su32(bars), bPre = su32(bars + 1), bNorm = su32(bars + 2);
-    auto bGrp = [&](int j) { return su32(bars + 3 + j); };  // copy j's slices are in
     const bool norm = p.rms_w != nullptr && !mixes_only;
     const int64_t F = 4LL * p.d;
 
     // Each barrier completes once: recv when the 16 records of this CTA's
     // token are in (owners only), pre when pre of all tv tokens is in, norm
-    // (with the RMSNorm) when every CTA's partial sum of y^2 of every token
-    // is, grp(j) when copy j's slices of W and x are in.
+    // (with the RMSNorm) when every CTA's partial sum of y^2 of every token is.
     if (threadIdx.x == 0) {
         *abort_word = 0;
         mbar_init(bRecv, 1);
         mbar_init(bPre, 1);
         mbar_init(bNorm, 1);
-        for (int j = 0; j < 4; ++j) mbar_init(bGrp(j), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (rank < tv) mbar_expect_tx(bRecv, kCluster * kRecVals * 4);
         if (!mixes_only) mbar_expect_tx(bPre, (uint32_t)tv * 16);
         if (norm) mbar_expect_tx(bNorm, (uint32_t)(kCluster * tv * 4));
-        for (int j = 0; j < 4; ++j)
-            mbar_expect_tx(bGrp(j), (uint32_t)(kMix * w * 4 + tv * w * 2));
-    }
-    // W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) and x slice
-    // (token t, copy j -> x[tok0+t][j][r*w ...], w bf16) by bulk copies
-    // from warp 0, copy j before copy j+1, so that the projection of copy j
-    // starts as soon as its barrier completes.  Rows up to the next multiple
-    // of 4 tokens are zero.
-    const int tz = round4(tv);
-    if (warp == 0) {
-        __syncwarp();  // the barriers are initialised and armed
-        for (int j = 0; j < 4; ++j)
-            for (int e = lane; e < kMix + tv; e += 32) {
-                if (e < kMix)
-                    bulk_g2s(su32(ws + e * nf + j * w),
-                             p.w_mix + (int64_t)e * F + (int64_t)j * p.d + rank * w,
-                             (uint32_t)(w * 4), bGrp(j));
-                else
-                    bulk_g2s(su32(xs + (e - kMix) * nf + j * w),
-                             p.x + ((tok0 + (e - kMix)) * 4 + j) * (int64_t)p.d + rank * w,
-                             (uint32_t)(w * 2), bGrp(j));
-            }
-    } else {
-        const int xv = w / 8;
-        for (int e = threadIdx.x - 32; e < (tz - tv) * 4 * xv; e += kThreads - 32) {
-            const int t = tv + e / (4 * xv), q = e % (4 * xv);
-            *reinterpret_cast<uint4 *>(xs + t * nf + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
-        }
     }
     cluster_arrive();  // waited for before the first remote store
-    __syncthreads();   // the zero rows are written
+
+    // W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) and x slice
+    // (token t, copy j -> x[tok0+t][j][r*w ...]) as asynchronous copies, one
+    // group per copy j, so that the projection of copy j starts as soon as
+    // its group is in.  Rows up to the next multiple of 4 tokens are zero.
+    // Rows by warp, 16-byte pieces by lane: no division in the index math.
+    {
+        const int wv = w / 4, xv = w / 8, tz = round4(tv);
+        for (int j = 0; j < 4; ++j) {
+            for (int i = warp; i < kMix; i += kWarps) {
+                const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
+                const uint32_t dst = su32(ws + i * nf + j * w);
+                for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
+            }
+            for (int t = warp; t < tz; t += kWarps) {
+                uint16_t *dst = xs + t * nf + j * w;
+                if (t < tv) {
+                    const uint16_t *src = p.x + ((tok0 + t) * 4 + j) * (int64_t)p.d + rank * w;
+                    for (int q = lane; q < xv; q += 32) cp_async16(su32(dst + 8 * q), src + 8 * q);
+                } else {
+                    for (int q = lane; q < xv; q += 32)
+                        *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            cp_async_commit();
+        }
+    }
 
     // Partial mix numbers (and sums of squares, h == 0) of tokens 4g..4g+3,
     // as pairs (even feature, odd feature) summed at the end.
@@ -195,13 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
 #pragma unroll
         for (int k = 0; k < 6; ++k) acc[u][k] = 0;
     }
-    bool landed = true;
     for (int j = 0; j < 4; ++j) {
-        if (!wait_bar<false>(bGrp(j), 0, abort, p.err)) {
-            landed = false;
-            break;
-        }
+        cp_async_wait(3 - j);
+        __syncthreads();  // every thread's copies of group j are in
         if (!active) continue;
+        // unrolled, so that the loads of several feature blocks are in
+        // flight together (the loop is bound by shared-memory latency)
+#pragma unroll 5
         for (int f = j * w + 2 * lane; f < (j + 1) * w; f += 64) {
             uint64_t wv[6];
 #pragma unroll
@@ -276,17 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
                 if (lane < kCluster)
                     st_async_v4(mapa(su32(preb + rank * 4), (uint32_t)lane), pr[0], pr[1], pr[2],
                                 pr[3], mapa(bPre, (uint32_t)lane));
+                // comb: entry (j, k) on lane 4j + k of each half-warp
+                const int ce = 8 + (lane & 15);
+                const float c = sinkhorn_comb4_lanes(
+                    fmaf(__shfl_sync(0xFFFFFFFFu, m, ce), s2, __ldg(p.base + ce)), p.iters, p.eps);
+                if (lane < 16) p.comb[t * 16 + lane] = c;
                 if (lane == 0) {
-                    float Cm[4][4];
-                    sinkhorn_comb<4>([&](int k) { return mm[k]; },
-                                     [&](int k) { return bse[k]; }, s2, p.iters, p.eps, Cm);
                     reinterpret_cast<float4 *>(p.pre)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
                     reinterpret_cast<float4 *>(p.post)[t] =
                         make_float4(po[0], po[1], po[2], po[3]);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
-                            make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
                 }
             }
         }
@@ -359,10 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         }
     }
 
-    // No bulk copy may still be writing this CTA's shared memory at exit
-    // (this matters only after an abort: otherwise every thread waited).
-    if (!landed && threadIdx.x == 0)
-        for (int j = 0; j < 4; ++j) drain_bar(bGrp(j), 0);
     // A CTA that took a store from another CTA waited for it above, so no
     // store is still in flight toward a CTA that passes this barrier: the
     // barrier needs no release (pending global stores need not drain).

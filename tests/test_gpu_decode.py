@@ -132,6 +132,23 @@ def test_decode_agrees_with_other_paths(hc, path):
     assert bool(((y.float() - y2.float()).abs() <= bound).all())
 
 
+@pytest.mark.parametrize("iters", [1, 20, 50])
+def test_decode_coefficients_equal_the_split_kernel_on_its_own_mixes(hc, iters):
+    # The owner runs the Sinkhorn on 16 lanes (one comb entry each); it must
+    # give bit for bit what the one-token-per-thread split kernel gives for
+    # the same mix numbers (same operations on the same values, in the same
+    # pairwise order).  Large logit scales reach the eps-dominated corners.
+    n, d = 64, 5120
+    x, w, sc, base = case(n, d, 40 + iters)
+    sc = sc * 20
+    y, pre, post, comb, m, launches = run(hc, x, w, sc, base, iters=iters)
+    assert launches == 1
+    pre2, post2, comb2 = hc.hc_split_sinkhorn(m, sc, base, 4, iters, 1e-6)
+    torch.cuda.synchronize()
+    for a, b in ((pre, pre2), (post, post2), (comb, comb2)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
 def test_decode_repeated_calls_are_deterministic(hc):
     x, w, sc, base = case(100, 5120, 4)
     a = run(hc, x, w, sc, base)
