@@ -177,36 +177,6 @@ __device__ __forceinline__ void sinkhorn_comb(MixFn m, BaseFn base, float s2, in
     }
 }
 
-// The same comb for HC = 4, spread over a 16-lane group of the warp: lane
-// 4j + k (of the group) holds L_jk on entry and C_jk on return.  Row sums
-// combine lanes 4j..4j+3 and column sums lanes k, k+4, k+8, k+12 by xor
-// shuffles in the pairwise order of sinkhorn_comb, and every other step is
-// the same operation on the same value, so the result is bit-identical to
-// sinkhorn_comb<4>; one step's dependency chain is one entry's instead of
-// four rows' (or columns') in turn.  All 32 lanes of the warp must call it.
-__device__ __forceinline__ float sinkhorn_comb4_lanes(float L, int iters, float eps) {
-    constexpr unsigned kAll = 0xFFFFFFFFu;
-    float mx = fmaxf(L, __shfl_xor_sync(kAll, L, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(kAll, mx, 2));
-    const float e = expf(L - mx);
-    float s = e + __shfl_xor_sync(kAll, e, 1);
-    s = s + __shfl_xor_sync(kAll, s, 2);
-    float c = fmaf(e, rcp_refined(s), eps);
-    auto col_step = [&]() {
-        float t = c + __shfl_xor_sync(kAll, c, 4);
-        t = t + __shfl_xor_sync(kAll, t, 8);
-        c *= rcp_refined(t + eps);
-    };
-    col_step();
-    for (int it = 1; it < iters; ++it) {
-        float t = c + __shfl_xor_sync(kAll, c, 1);
-        t = t + __shfl_xor_sync(kAll, t, 2);
-        c *= rcp_refined(t + eps);
-        col_step();
-    }
-    return c;
-}
-
 // One token: m = its (2+HC)*HC mix numbers, s0..s2 = hc_scale, base = hc_base.
 template <int HC, typename MixFn, typename BaseFn>
 __device__ __forceinline__ void split_sinkhorn_token(MixFn m, BaseFn base, float s0, float s1,

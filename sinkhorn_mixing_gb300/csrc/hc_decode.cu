@@ -22,7 +22,7 @@
 //     with asynchronous 4-byte stores whose bytes complete the owner's
 //     barrier.  The owner sums the 16 records in CTA order, forms r, m and
 //     pre, sends pre to all 16 CTAs the same way and then runs the Sinkhorn
-//     for comb on 16 lanes, one comb entry each.
+//     for comb.
 //   * Every CTA collapses its own w channels of the cluster's tokens from the
 //     x slice it holds, so x is read from memory once.
 //
@@ -268,15 +268,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
                 if (lane < kCluster)
                     st_async_v4(mapa(su32(preb + rank * 4), (uint32_t)lane), pr[0], pr[1], pr[2],
                                 pr[3], mapa(bPre, (uint32_t)lane));
-                // comb: entry (j, k) on lane 4j + k of each half-warp
-                const int ce = 8 + (lane & 15);
-                const float c = sinkhorn_comb4_lanes(
-                    fmaf(__shfl_sync(0xFFFFFFFFu, m, ce), s2, __ldg(p.base + ce)), p.iters, p.eps);
-                if (lane < 16) p.comb[t * 16 + lane] = c;
+                // comb on one lane: spread over 16 lanes (one entry each,
+                // shuffle row and column sums) it measured slower, a shuffle
+                // costing more than the three other rows' steps it saves
                 if (lane == 0) {
+                    float Cm[4][4];
+                    sinkhorn_comb<4>([&](int k) { return mm[k]; },
+                                     [&](int k) { return bse[k]; }, s2, p.iters, p.eps, Cm);
                     reinterpret_cast<float4 *>(p.pre)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
                     reinterpret_cast<float4 *>(p.post)[t] =
                         make_float4(po[0], po[1], po[2], po[3]);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
+                            make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
                 }
             }
         }

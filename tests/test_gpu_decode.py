@@ -134,10 +134,10 @@ def test_decode_agrees_with_other_paths(hc, path):
 
 @pytest.mark.parametrize("iters", [1, 20, 50])
 def test_decode_coefficients_equal_the_split_kernel_on_its_own_mixes(hc, iters):
-    # The owner runs the Sinkhorn on 16 lanes (one comb entry each); it must
-    # give bit for bit what the one-token-per-thread split kernel gives for
-    # the same mix numbers (same operations on the same values, in the same
-    # pairwise order).  Large logit scales reach the eps-dominated corners.
+    # The decode kernel's owner lane must give bit for bit what the
+    # one-token-per-thread split kernel gives for the same mix numbers (the
+    # same operations on the same values, in the same order).  Large logit
+    # scales reach the eps-dominated corners.
     n, d = 64, 5120
     x, w, sc, base = case(n, d, 40 + iters)
     sc = sc * 20
