@@ -218,7 +218,9 @@ size_t hc_workspace_bytes(int64_t n, int hc, int64_t d);
 /*
  * hc_device_error -- reads the error word of the current CUDA device:
  * bit 0 set = a kernel gave up on a bounded wait (its outputs for the
- * affected tile are not valid).  Synchronises the device.  With clear != 0
+ * affected tile are not valid); bit 1 set = a fused kernel found its shared
+ * memory not on a 1024-byte boundary and did no work (its outputs are not
+ * valid).  Synchronises the device.  With clear != 0
  * the word is reset to 0 afterwards.  flags may be NULL (then only clears).
  */
 hc_status hc_device_error(unsigned int *flags, int clear);

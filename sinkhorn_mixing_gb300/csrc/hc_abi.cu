@@ -350,15 +350,15 @@ hc_status mixes_pre_impl(int64_t n, int hc, int64_t d, int iters, float eps, flo
                                            di, s));
     }
     if (hc::fused_supported(hc, d, di)) {
-        // With the RMSNorm: the fused kernel, then one pass over its rows.  A
-        // second pass inside the fused kernel lengthened the chain that bounds
-        // it (1.33 ms against 0.69 ms at 65,536 tokens, d = 5120); the
-        // separate pass moves 2 x 10 KB per token.
-        cudaError_t e = hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
-                                         hc_base, mixes, pre, post, comb, y, di, s);
-        if (e == cudaSuccess && rms_w != nullptr)
-            e = hc::launch_rmsnorm(n, d, y, rms_w, rms_eps, di, s);
-        return from_cuda(e);
+        // With the RMSNorm: the same kernel with the norm folded into the
+        // collapse (its statistic from the copies' Gram matrix, so no second
+        // pass over the rows).
+        return from_cuda(rms_w == nullptr
+                             ? hc::launch_fused(n, hc, d, iters, eps, norm_eps, x, w_mix, hc_scale,
+                                                hc_base, mixes, pre, post, comb, y, di, s)
+                             : hc::launch_fused_norm(n, hc, d, iters, eps, norm_eps, x, w_mix,
+                                                     hc_scale, hc_base, mixes, pre, post, comb, y,
+                                                     rms_w, rms_eps, di, s));
     }
     // General path: three kernels, the mix numbers passing through m.  A
     // workspace with room past the mix numbers (hc_workspace_bytes) also

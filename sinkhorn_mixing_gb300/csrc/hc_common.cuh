@@ -14,6 +14,7 @@ namespace hc {
 
 // Error word bits (per device, read by hc_device_error).
 constexpr unsigned int kErrWaitTimeout = 1u;
+constexpr unsigned int kErrSmemLayout = 2u;  // shared memory base off its 1024-byte boundary
 
 // ---------------------------------------------------------------- bf16
 

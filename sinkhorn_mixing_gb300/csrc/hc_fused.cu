@@ -63,9 +63,16 @@ constexpr int kSubBytes = kTM * 128;     // one swizzled [64 tokens x 64 channel
 constexpr int kStageBytes = 4 * kSubBytes;  // the 4 copies' sub-tiles of one chunk
 constexpr int kWChunkBytes = kNW * 128;  // one [48 x 64] bf16 chunk of W
 constexpr int kOwn = kTM / kCluster;     // tokens owned per CTA per tile
-constexpr int kRec = 28;                 // floats per partial record (24 + ssq + pad)
+// floats per partial record: 24 mix partials, the sum of squares, and with
+// the RMSNorm the 10 entries G_jk (j <= k) of the copies' Gram matrix
+constexpr int kRec = 36;
+constexpr int kGram = 10;
 // bytes of records one owner receives per tile: 16 senders x 4 tokens x 7 x 16 B
-constexpr uint32_t kRecvTx = kCluster * kOwn * 7 * 16;
+// record bytes per sender and token: 6 x 16 (mixes) + 16 (sum of squares,
+// padded), or with the RMSNorm 6 x 16 + 4 + 40
+__host__ __device__ constexpr uint32_t recv_tx(bool norm) {
+    return kCluster * kOwn * (norm ? 6 * 16 + 4 + 4 * kGram : 7 * 16);
+}
 constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
 // The producer runs at most kLag tiles ahead of this CTA's collapse, which
@@ -146,6 +153,10 @@ struct FusedParams {
     const float *post_in;
     const float *comb_in;
     uint16_t *x_next;
+    // RMSNorm of the sublayer input (NORM variant only): y is written as
+    // RMSNorm(y) with weight rms_w [d]
+    const float *rms_w;
+    float rms_eps;
 };
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -193,7 +204,7 @@ struct Smem {
     uint8_t *w;       // 4*ncc chunks of [48 x 64] bf16, swizzled, chunk = copy*ncc + cc
     float *recv;      // [kCluster][kOwn][kRec]      partials received as owner
     float *sq;        // [2][kTM]                    this CTA's partial sums of squares
-    float *stage;     // [kColDoneBufs][kOwn][4]     pre of the owned tokens, by tile % 4
+    float *stage;     // [kColDoneBufs][kOwn][8]     pre (and the RMS factor) of the owned tokens, by tile % 4
     uint64_t *bar;    // barriers, see below
     uint32_t *tmem;   // TMEM base address written by tcgen05.alloc
     int *abort;
@@ -217,14 +228,18 @@ constexpr int kNumBars = kMmaDrain + 1 + kSlots;
 constexpr size_t kRingBytes = (size_t)kSlots * kStageBytes;
 constexpr size_t kRecvBytes = (size_t)kCluster * kOwn * kRec * 4;
 
+// The dynamic shared memory of a kernel with no static shared memory starts
+// on a 1024-byte boundary (the 128-byte swizzle atoms of the ring and W need
+// it); the kernel checks that and does no work if it does not hold.
 __host__ __device__ constexpr size_t smem_bytes(int ncc) {
-    return 1024 /* alignment slack */ + kRingBytes + (size_t)4 * ncc * kWChunkBytes + kRecvBytes +
-           2 * kTM * 4 + kColDoneBufs * kOwn * 4 * 4 + kNumBars * 8 + 16;
+    return kRingBytes + (size_t)4 * ncc * kWChunkBytes + kRecvBytes + 2 * kTM * 4 +
+           kColDoneBufs * kOwn * 8 * 4 + kNumBars * 8 + 16;
 }
 
+static_assert(smem_bytes(kMaxNcc) <= 232448, "over the 227 KB of shared memory per CTA");
+
 __device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
-    uintptr_t a = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~(uintptr_t)1023;
-    uint8_t *p = reinterpret_cast<uint8_t *>(a);
+    uint8_t *p = raw;
     Smem s;
     s.ring = p;
     p += kRingBytes;
@@ -237,7 +252,7 @@ __device__ __forceinline__ Smem carve(uint8_t *raw, int ncc) {
     s.sq = reinterpret_cast<float *>(p);
     p += 2 * kTM * 4;
     s.stage = reinterpret_cast<float *>(p);
-    p += kColDoneBufs * kOwn * 4 * 4;
+    p += kColDoneBufs * kOwn * 8 * 4;
     s.bar = reinterpret_cast<uint64_t *>(p);
     p += kNumBars * 8;
     s.tmem = reinterpret_cast<uint32_t *>(p);
@@ -257,12 +272,14 @@ __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams
 
 // NCC = w / 64 (64-channel sub-tiles per copy per CTA) is a template
 // parameter so that all index arithmetic is by constants.
-template <int NCC, bool POST>
+template <int NCC, bool POST, bool NORM>
 __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_xn,
             const __grid_constant__ CUtensorMap tmap_out, const FusedParams p) {
     using R = Roles<POST>;
     constexpr int kThreads = R::kThreads;
+    static_assert(!(POST && NORM), "hc_post in front and the RMSNorm behind are separate variants");
+    constexpr uint32_t kRecvTx = recv_tx(NORM);
     extern __shared__ uint8_t smem_raw[];
     constexpr int ncc = NCC;
     const Smem sm = carve(smem_raw, ncc);
@@ -271,13 +288,18 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
     const int cluster = (int)(blockIdx.x / kCluster);
     const int nclusters = (int)(gridDim.x / kCluster);
     const bool mixes_only = p.mixes_only != 0;
-    const int T = cluster < p.num_tiles ? (p.num_tiles - cluster + nclusters - 1) / nclusters : 0;
+    // off its 1024-byte boundary the layout would not fit: no tiles then
+    const bool aligned = (su32(smem_raw) & 1023u) == 0;
+    const int T = cluster < p.num_tiles && aligned
+                      ? (p.num_tiles - cluster + nclusters - 1) / nclusters
+                      : 0;
     volatile int *abort = sm.abort;
     auto bar = [&](int i) { return su32(sm.bar + i); };
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
         *abort = 0;
+        if (!aligned) atomicOr(p.err, kErrSmemLayout);
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(bar(bFull(s)), 1);
             mbar_init(bar(bEmpty(s)), R::kEmptyArrivals);
@@ -535,6 +557,11 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
             for (int a2 = 0; a2 < PP / 2; ++a2)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) s2[a2][e] = 0;
+            // NORM: the copies' Gram matrix G_jk = sum_c x_jc x_kc of this
+            // thread's channels, entries j <= k in row order, packed pairs
+            uint64_t g2[NORM ? kGram : 1];
+#pragma unroll
+            for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) g2[q2] = 0;
             if (POST) {
                 const int64_t tok = (int64_t)tile_of((uint32_t)(ncc * it)) * kTM + i;
                 float4 pv = make_float4(0.f, 0.f, 0.f, 0.f), cv[4];
@@ -565,7 +592,7 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 auto piece = [&](int j, int m) -> uint32_t {
                     return base + j * kSubBytes + (((PP * part + m) ^ (i & 7)) << 4);
                 };
-                if (!POST) {
+                if (!POST && !NORM) {
 #pragma unroll
                     for (int m = 0; m < PP; ++m)
 #pragma unroll
@@ -580,6 +607,38 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                         }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
+                } else if (!POST) {
+                    // the same squares in the same order, and the Gram
+                    // entries of the piece's four copies
+#pragma unroll
+                    for (int m = 0; m < PP; ++m) {
+                        uint32_t wv[4][4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 v = lds128(piece(j, m));
+                            wv[j][0] = v.x, wv[j][1] = v.y, wv[j][2] = v.z, wv[j][3] = v.w;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const uint64_t xp = bf16x2_to_f32x2(wv[j][e]);
+                                ffma2(s2[m / 2][e], xp, xp);
+                            }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint64_t xp[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) xp[j] = bf16x2_to_f32x2(wv[j][e]);
+                            int q2 = 0;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                                for (int k = j; k < 4; ++k) ffma2(g2[q2++], xp[j], xp[k]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(bEmpty(slot)));
                 } else {
                     // hc_post ("Mix projection" page, Block.hc_post) of this
                     // thread's channels of the stage, one 8-channel piece at a
@@ -587,7 +646,7 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                     // product first, then the copies j = 0..3 in order (as
                     // hc_post); written back over the residual in the slot
                     // (all four input copies of a piece are read before any is
-                    // written).  The store thread writes the slot to x_next.
+                    // written).  The MMA thread stores the slot to x_next.
                     uint4 ocur[PP];
 #pragma unroll
                     for (int m = 0; m < PP; ++m) ocur[m] = onext[m];
@@ -655,6 +714,33 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
             if (part == 0) sm.sq[b * kTM + i] = ss;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bSqFull(b)));
+            if (NORM) {
+                // the row's Gram entries go straight into its owner's record
+                // (floats 25..34), once the owner has read the previous
+                // tile's records; their bytes complete its recv_full
+                float gs[kGram];
+#pragma unroll
+                for (int q2 = 0; q2 < kGram; ++q2) {
+                    gs[q2] = sum2(g2[q2]);
+#pragma unroll
+                    for (int sh = 1; sh < LP; sh <<= 1)
+                        gs[q2] += __shfl_xor_sync(0xFFFFFFFFu, gs[q2], sh);
+                }
+                if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(kRecvFree), ((uint32_t)it & 1) ^ 1,
+                                                            abort, p.err)))
+                    break;
+                if (part == 0) {
+                    const int owner = i / kOwn, u = i % kOwn;
+                    const uint32_t rec =
+                        mapa(su32(sm.recv + (rank * kOwn + u) * kRec), (uint32_t)owner);
+                    const uint32_t rfull = mapa(bar(kRecvFull), (uint32_t)owner);
+                    st_async_f32(rec + 100, gs[0], rfull);
+                    st_async_v2(rec + 104, gs[1], gs[2], rfull);
+                    st_async_v4(rec + 112, gs[3], gs[4], gs[5], gs[6], rfull);
+                    st_async_v2(rec + 128, gs[7], gs[8], rfull);
+                    st_async_f32(rec + 136, gs[9], rfull);
+                }
+            }
         }
     } else if (warp == kWarpEpi0 || warp == kWarpEpi0 + 1) {
         // TMEM lanes 32*(warp%4) .. +31 = tokens of the tile
@@ -694,7 +780,10 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                             acc[4 * v + 1] + acc[24 + 4 * v + 1],
                             acc[4 * v + 2] + acc[24 + 4 * v + 2],
                             acc[4 * v + 3] + acc[24 + 4 * v + 3], rfull);
-            st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
+            if (NORM)
+                st_async_f32(rec + 96, ss, rfull);  // the Gram entries follow
+            else
+                st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
         }
     } else if (warp == kWarpOwner) {
         // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: lanes u < kOwn
@@ -716,6 +805,9 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 break;
             float m[kMix];
             float ssum = 0.f;
+            float G[NORM ? kGram : 1];  // NORM: the token's Gram entries over all d
+#pragma unroll
+            for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) G[q2] = 0.f;
             if (lane < kOwn) {
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) m[k] = 0.f;
@@ -730,7 +822,15 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                         m[4 * v + 2] += t4.z;
                         m[4 * v + 3] += t4.w;
                     }
-                    ssum += r4[6].x;
+                    const float4 t6 = r4[6];
+                    ssum += t6.x;
+                    if (NORM) {
+                        const float4 t7 = r4[7], t8 = r4[8];
+                        const float gv[kGram] = {t6.y, t6.z, t6.w, t7.x, t7.y,
+                                                 t7.z, t7.w, t8.x, t8.y, t8.z};
+#pragma unroll
+                        for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) G[q2] += gv[q2];
+                    }
                 }
             }
             float pr[4], po[4];
@@ -752,8 +852,26 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                     // (the producer stays at most kLag = 3 tiles ahead).
                     split_pre_post<4>([&](int k) { return m[k]; }, [&](int k) { return bse[k]; },
                                       s0, s1, p.eps, pr, po);
-                    reinterpret_cast<float4 *>(sm.stage)[(it % kColDoneBufs) * kOwn + lane] =
-                        make_float4(pr[0], pr[1], pr[2], pr[3]);
+                    float rs = 0.f;
+                    if (NORM) {
+                        // RMSNorm statistic of the collapse y = sum_j pre_j x_j
+                        // over all d channels: sum_c y_c^2 = pre^T G pre (of
+                        // the binary32 collapse, before its bf16 rounding)
+                        float q = 0.f;
+                        int q2 = 0;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int k = j; k < 4; ++k, ++q2)
+                                q = fmaf((k == j ? 1.f : 2.f) * pr[j] * pr[k], G[q2 % (NORM ? kGram : 1)], q);
+                        rs = rsqrtf(fmaxf(q, 0.f) / (float)p.d + p.rms_eps);
+                    }
+                    // the collapse weights pre, and with NORM the token's
+                    // RMSNorm factor
+                    float4 *st4 =
+                        reinterpret_cast<float4 *>(sm.stage) + 2 * ((it % kColDoneBufs) * kOwn + lane);
+                    st4[0] = make_float4(pr[0], pr[1], pr[2], pr[3]);
+                    if (NORM) st4[1] = make_float4(rs, 0.f, 0.f, 0.f);
                 }
             }
             __syncwarp();
@@ -795,6 +913,22 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
         constexpr int nv = NCC * 8 * kCluster;  // vectors per copy row (d / 8)
         constexpr int nout = kOwn * nv;
         const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
+        // NORM: the RMSNorm weight of this thread's vectors v = ct + 224 k,
+        // held for the whole launch
+        constexpr int kNormV = NORM ? (nv + kCollapseThreads - 1) / kCollapseThreads : 1;
+        float gw[kNormV][8];
+#pragma unroll
+        for (int k = 0; k < kNormV; ++k) {
+            const int v = ct + k * kCollapseThreads;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) gw[k][e] = 0.f;
+            if (NORM && v < nv) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v);
+                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v + 1);
+                gw[k][0] = g0.x, gw[k][1] = g0.y, gw[k][2] = g0.z, gw[k][3] = g0.w;
+                gw[k][4] = g1.x, gw[k][5] = g1.y, gw[k][6] = g1.z, gw[k][7] = g1.w;
+            }
+        }
         for (int it = 0; it < T; ++it) {
             const int tile = cluster + it * nclusters;
             const int ib = it % kColDoneBufs;
@@ -803,40 +937,89 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                                                          p.err)))
                 break;
             const int64_t tok0 = (int64_t)tile * kTM + rank * kOwn;
-            constexpr int G = POST ? 3 : 4;  // 96 registers with POST
-            for (int o0 = ct; o0 < nout; o0 += G * kCollapseThreads) {
-                uint4 xv[G][4];
+            if (NORM) {
+                // vector v (8 channels) of all kOwn tokens per step, so that
+                // the weight held for v serves the four of them:
+                // y = bf16((bf16(sum_j pre_j x_j) g) r)
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int o = o0 + g * kCollapseThreads;
-                    const int64_t tok = tok0 + o / nv;
-                    if (o < nout && tok < p.n) {
+                for (int k = 0; k < kNormV; ++k) {
+                    const int v = ct + k * kCollapseThreads;
+                    if (v >= nv) break;
+                    uint4 xv[kOwn][4];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            xv[g][j] = __ldcs(x + (tok * 4 + j) * nv + o % nv);
+                    for (int u = 0; u < kOwn; ++u) {
+                        const int64_t tok = tok0 + u;
+                        if (tok < p.n) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) xv[u][j] = __ldcs(x + (tok * 4 + j) * nv + v);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kOwn; ++u) {
+                        const int64_t tok = tok0 + u;
+                        if (tok < p.n) {
+                            const float4 *st4 =
+                                reinterpret_cast<const float4 *>(sm.stage) + 2 * (ib * kOwn + u);
+                            const float4 pr = st4[0];
+                            const float rs = st4[1].x;
+                            float acc[8], f[8];
+                            unpack8(xv[u][0], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
+                            unpack8(xv[u][1], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
+                            unpack8(xv[u][2], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
+                            unpack8(xv[u][3], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
+                            // the collapse in bf16 (as hc_pre writes it), then
+                            // the RMSNorm: (y g) r
+                            unpack8(pack8(acc), f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = (f[e] * gw[k][e]) * rs;
+                            st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + v, pack8(acc));
+                        }
                     }
                 }
+            } else {
+                constexpr int G = POST ? 3 : 4;  // 96 registers with POST
+                for (int o0 = ct; o0 < nout; o0 += G * kCollapseThreads) {
+                    uint4 xv[G][4];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const int o = o0 + g * kCollapseThreads;
-                    const int64_t tok = tok0 + o / nv;
-                    if (o < nout && tok < p.n) {
-                        const float4 pr = reinterpret_cast<const float4 *>(
-                            sm.stage)[ib * kOwn + o / nv];
-                        float acc[8], f[8];
-                        unpack8(xv[g][0], f);
+                    for (int g = 0; g < G; ++g) {
+                        const int o = o0 + g * kCollapseThreads;
+                        const int64_t tok = tok0 + o / nv;
+                        if (o < nout && tok < p.n) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
-                        unpack8(xv[g][1], f);
+                            for (int j = 0; j < 4; ++j)
+                                xv[g][j] = __ldcs(x + (tok * 4 + j) * nv + o % nv);
+                        }
+                    }
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
-                        unpack8(xv[g][2], f);
+                    for (int g = 0; g < G; ++g) {
+                        const int o = o0 + g * kCollapseThreads;
+                        const int64_t tok = tok0 + o / nv;
+                        if (o < nout && tok < p.n) {
+                            const float4 pr = reinterpret_cast<const float4 *>(
+                                sm.stage)[2 * (ib * kOwn + o / nv)];
+                            float acc[8], f[8];
+                            unpack8(xv[g][0], f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
-                        unpack8(xv[g][3], f);
+                            for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
+                            unpack8(xv[g][1], f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
-                        st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + o % nv, pack8(acc));
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
+                            unpack8(xv[g][2], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
+                            unpack8(xv[g][3], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
+                            st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + o % nv, pack8(acc));
+                        }
                     }
                 }
             }
@@ -872,15 +1055,21 @@ DevState g_dev[64];
 
 using FusedKernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, FusedParams);
 
-// The instantiation for w = 64 * ncc channels per CTA (POST: with the
-// previous sublayer's hc_post in front).
-FusedKernel kernel_for(int ncc, bool post) {
+// The instantiation for w = 64 * ncc channels per CTA (post: with the
+// previous sublayer's hc_post in front; norm: with the RMSNorm of the
+// collapse behind; not both).
+template <int NCC>
+FusedKernel kernel_ncc(bool post, bool norm) {
+    return post ? k_fused<NCC, true, false> : norm ? k_fused<NCC, false, true>
+                                                   : k_fused<NCC, false, false>;
+}
+FusedKernel kernel_for(int ncc, bool post, bool norm = false) {
     switch (ncc) {
-        case 1: return post ? k_fused<1, true> : k_fused<1, false>;
-        case 2: return post ? k_fused<2, true> : k_fused<2, false>;
-        case 3: return post ? k_fused<3, true> : k_fused<3, false>;
-        case 4: return post ? k_fused<4, true> : k_fused<4, false>;
-        default: return post ? k_fused<5, true> : k_fused<5, false>;
+        case 1: return kernel_ncc<1>(post, norm);
+        case 2: return kernel_ncc<2>(post, norm);
+        case 3: return kernel_ncc<3>(post, norm);
+        case 4: return kernel_ncc<4>(post, norm);
+        default: return kernel_ncc<5>(post, norm);
     }
 }
 
@@ -896,12 +1085,13 @@ const DevState &dev_state(const DeviceInfo &di) {
     if (prop.major != 10 || prop.minor != 3) return st;  // built for sm_103a only
     if (tensor_map_encoder() == nullptr) return st;
     for (int ncc = 1; ncc <= kMaxNcc; ++ncc)
-        for (int post = 0; post < 2; ++post) {
-            if (cudaFuncSetAttribute(kernel_for(ncc, post), cudaFuncAttributeMaxDynamicSharedMemorySize,
+        for (int v = 0; v < 3; ++v) {  // plain, post, norm
+            const FusedKernel k = kernel_for(ncc, v == 1, v == 2);
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)smem_bytes(ncc)) != cudaSuccess)
                 return st;
-            if (cudaFuncSetAttribute(kernel_for(ncc, post),
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            if (cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess)
                 return st;
         }
     for (int post = 0; post < 2; ++post) {
@@ -946,10 +1136,12 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
                         const float *scale, const float *base, float *mixes, float *pre,
                         float *post, float *comb, uint16_t *y, const uint16_t *out,
                         const float *post_in, const float *comb_in, uint16_t *x_next,
-                        const DeviceInfo &di, cudaStream_t s) {
+                        const float *rms_w, float rms_eps, const DeviceInfo &di,
+                        cudaStream_t s) {
     const DevState &st = dev_state(di);
     if (!st.ok || n >= (int64_t(1) << 31)) return cudaErrorNotSupported;
-    const bool with_post = out != nullptr;
+    const bool with_post = out != nullptr, with_norm = rms_w != nullptr;
+    if (with_post && with_norm) return cudaErrorNotSupported;
     const int64_t F = 4 * d;
     const int ncc = (int)(d / (kCluster * 64));
     // 4-D view of x: {64 channels, token, 64-channel chunk of a copy, copy};
@@ -1010,6 +1202,8 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
     p.post_in = post_in;
     p.comb_in = comb_in;
     p.x_next = x_next;
+    p.rms_w = rms_w;
+    p.rms_eps = rms_eps;
     const int mc = st.max_clusters[with_post ? 1 : 0];
     const int nclusters = p.num_tiles < mc ? p.num_tiles : mc;
     cudaLaunchConfig_t cfg = {};
@@ -1024,7 +1218,8 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc, with_post), tmap, tmap_xn, tmap_out, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel_for(p.ncc, with_post, with_norm), tmap, tmap_xn,
+                                             tmap_out, p);
     if (e != cudaSuccess) return e;
     return launched();
 }
@@ -1037,7 +1232,17 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
                          uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
     if (hc != 4) return cudaErrorNotSupported;
     return launch_impl(n, d, iters, eps, norm_eps, x, x, w, scale, base, mixes, pre, post, comb,
-                       y, nullptr, nullptr, nullptr, nullptr, di, s);
+                       y, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f, di, s);
+}
+
+cudaError_t launch_fused_norm(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                              const uint16_t *x, const float *w, const float *scale,
+                              const float *base, float *mixes, float *pre, float *post,
+                              float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                              const DeviceInfo &di, cudaStream_t s) {
+    if (hc != 4 || pre == nullptr || rms_w == nullptr) return cudaErrorNotSupported;
+    return launch_impl(n, d, iters, eps, norm_eps, x, x, w, scale, base, mixes, pre, post, comb,
+                       y, nullptr, nullptr, nullptr, nullptr, rms_w, rms_eps, di, s);
 }
 
 cudaError_t launch_fused_post(int64_t n, int hc, int64_t d, const uint16_t *out,
@@ -1048,7 +1253,7 @@ cudaError_t launch_fused_post(int64_t n, int hc, int64_t d, const uint16_t *out,
                               float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
     if (hc != 4 || pre == nullptr) return cudaErrorNotSupported;
     return launch_impl(n, d, iters, eps, norm_eps, residual, x_next, w, scale, base, mixes, pre,
-                       post, comb, y, out, post_in, comb_in, x_next, di, s);
+                       post, comb, y, out, post_in, comb_in, x_next, nullptr, 0.f, di, s);
 }
 
 }  // namespace hc

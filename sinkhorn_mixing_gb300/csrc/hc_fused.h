@@ -21,6 +21,15 @@ cudaError_t launch_fused(int64_t n, int hc, int64_t d, int iters, float eps, flo
                          const float *base, float *mixes, float *pre, float *post, float *comb,
                          uint16_t *y, const DeviceInfo &di, cudaStream_t s);
 
+// launch_fused with the RMSNorm of the collapse (weight rms_w [d], rms_eps)
+// applied before y is written: y = bf16((bf16(sum_j pre_j x_j) rms_w) r), r
+// the RMS factor of the binary32 collapse over all d channels.
+cudaError_t launch_fused_norm(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                              const uint16_t *x, const float *w, const float *scale,
+                              const float *base, float *mixes, float *pre, float *post,
+                              float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                              const DeviceInfo &di, cudaStream_t s);
+
 // hc_post of the previous sublayer followed by hc_mixes_pre on its result,
 // in one launch: x_next = hc_post(out, residual, post_in, comb_in) is written
 // (x_next may be residual itself), and pre, post, comb, y (and mixes when not

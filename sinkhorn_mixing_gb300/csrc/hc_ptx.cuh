@@ -106,6 +106,15 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
         : "memory");
 }
 
+// Asynchronous 8-byte store into another CTA's shared memory (as above).
+__device__ __forceinline__ void st_async_v2(uint32_t addr, float a, float b, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            addr),
+        "f"(a), "f"(b), "r"(bar)
+        : "memory");
+}
+
 // Asynchronous 4-byte store into another CTA's shared memory (as above).
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(

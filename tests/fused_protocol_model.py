@@ -20,7 +20,9 @@ the kernel's roles as generators that yield the barrier waits they make:
             of squares through sq_full / sq_empty; with `post` (x8) they
             first rewrite the stage in place (hc_post of the previous
             sublayer) and signal post_done, and leave the release to the MMA
-            thread;
+            thread; with `norm` each also waits until the previous tile's
+            records were read (recv_free) and sends its rows' Gram entries
+            into their owners' records, completing recv_full by bytes;
   epi (x2)  read the accumulator and the squares, wait until the previous
             tile's records were read (recv_free), then send their records to
             the owners, whose recv_full they complete by bytes;
@@ -104,11 +106,12 @@ STEP = ("step",)
 
 
 def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_only=False,
-             seed=0, mutation=None, post=False):
+             seed=0, mutation=None, post=False, norm=False):
     """Run one random interleaving; raises ProtocolError on any violation.
     `mutation` plants a known protocol mistake (for the tests that show the
     model can fail): "release_before_read", "empty_parity", and with post
-    "mma_waits_full", "release_before_store_read", "visible_before_written"."""
+    "mma_waits_full", "release_before_store_read", "visible_before_written", and
+    with norm "gram_without_recv_free"."""
     rnd = random.Random(seed)
     events = []
 
@@ -121,6 +124,7 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
     cs = []
     for r in range(C):
         cs.append(dict(
+            rank=r,
             full=[Barrier("full", 1) for _ in range(S)],
             post_done=[Barrier("post_done", NSQ) for _ in range(S)],
             posted=[set() for _ in range(S)],
@@ -135,12 +139,13 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             sq_empty=[Barrier("sq_empty", 2) for _ in range(2)],
             sq=[[None] * NSQ, [None] * NSQ],
             recv_full=Barrier("recv_full", 1), recv_free=Barrier("recv_free", C),
-            recv=[None] * C, reading=[False],
+            recv=[None] * C, recv_g=[None] * C, reading=[False],
             pre_ready=[Barrier("pre_ready", 1) for _ in range(bufs)],
             col_done=[Barrier("col_done", 2) for _ in range(bufs)],
             stage=[None] * bufs, stage_readers=[0] * bufs))
+    per_round = 2 * C if norm else C  # records (and Gram entries) per round
     for c in cs:
-        c["recv_full"].expect_tx(C)  # one record per sender and round
+        c["recv_full"].expect_tx(per_round)
 
     def producer(c):
         for it in range(T):
@@ -245,6 +250,20 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             yield wait(c["sq_empty"][b], ((it >> 1) & 1) ^ 1)
             c["sq"][b][w] = it
             c["sq_full"][b].arrive()
+            if norm:
+                if mutation != "gram_without_recv_free":
+                    yield wait(c["recv_free"], (it & 1) ^ 1)
+                lo, hi = w * C // NSQ, (w + 1) * C // NSQ
+                for o in range(lo, hi):
+                    def deliver_g(o=o, it=it, rank=c["rank"]):
+                        oc = cs[o]
+                        if oc["reading"][0]:
+                            raise ProtocolError("Gram entries land while their owner reads")
+                        if oc["recv_g"][rank] is not None:
+                            raise ProtocolError("Gram entries overwrite unread ones")
+                        oc["recv_g"][rank] = it
+                        oc["recv_full"].complete_tx(1)
+                    later(deliver_g)
 
     def epi(c, rank, half):
         mine = range(half * C // 2, (half + 1) * C // 2) if C > 1 else range(1)
@@ -281,6 +300,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             yield wait(c["recv_full"], it & 1)
             if c["recv"] != [it] * C:
                 raise ProtocolError("owner of tile %d finds records %s" % (it, c["recv"]))
+            if norm and c["recv_g"] != [it] * C:
+                raise ProtocolError("owner of tile %d finds Gram entries %s" % (it, c["recv_g"]))
             if mutation == "release_before_read":
                 for d in cs:
                     later(lambda d=d: d["recv_free"].arrive())
@@ -294,7 +315,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                 c["stage"][i] = it
                 c["pre_ready"][i].arrive()
             c["recv"] = [None] * C
-            c["recv_full"].expect_tx(C)
+            c["recv_g"] = [None] * C
+            c["recv_full"].expect_tx(per_round)
             if mutation != "release_before_read":
                 for d in cs:
                     later(lambda d=d: d["recv_free"].arrive())

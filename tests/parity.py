@@ -116,3 +116,35 @@ def check_post_all(y_bits, out_bits, res_bits, post, comb, hc, what="hc_post y")
                                       comb[t0:t1])
         acc.add(compare.check_bf16(y_bits[t0:t1], want, mag, hc + 1, what))
     return acc.finish()
+
+
+def check_norm_all(y_bits, x_bits, pre, rms_w, hc, rms_eps=1e-20, what="normalised y"):
+    """The normalised collapse against the oracle's RMSNorm of the oracle's
+    collapse with the GPU's pre, every token.  The GPU's row may differ from
+    it by one bf16 step of the collapse (or, where the hc terms cancel, by hc
+    binary32 roundings of their magnitude), scaled by the norm factor, plus
+    one step of the output; away from cancellation more than 99.9% of the
+    elements are within one step."""
+    n = x_bits.shape[0]
+    g = np.abs(np.asarray(rms_w, dtype=np.float64))
+    count = near = 0
+    worst = 0.0
+    for t0 in range(0, n, CHUNK):
+        t1 = min(n, t0 + CHUNK)
+        _, yc_bits, mag = oracle.hc_pre(x_bits[t0:t1], pre[t0:t1])
+        out_want, want_bits = oracle.hc_rmsnorm(yc_bits, rms_w, rms_eps)
+        yc = oracle.bf16_bits_to_f64(yc_bits)
+        inv = 1.0 / np.sqrt((yc ** 2).mean(axis=1, keepdims=True) + rms_eps)
+        got = oracle.bf16_bits_to_f64(y_bits[t0:t1])
+        allowed = (g * inv * (compare.bf16_ulp(yc) + hc * 2.0 ** -24 * mag) +
+                   compare.bf16_ulp(out_want) + 1e-5 * np.abs(out_want))
+        err = np.abs(got - out_want)
+        assert np.all(err <= allowed), (t0, float((err / allowed).max()))
+        worst = max(worst, float((err / allowed).max()))
+        count += err.size
+        near += int(np.sum(np.abs(compare.bf16_key(y_bits[t0:t1]) -
+                                  compare.bf16_key(want_bits)) <= 1))
+    print("PARITY %s: %d elements, %d within one bf16 step (%.6f), worst error %.3f of the "
+          "allowance" % (what, count, near, near / count, worst))
+    assert near / count > 0.999
+    return near / count

@@ -43,6 +43,21 @@ def test_records_before_the_new_stream_is_written_are_caught(stages):
                   mutation="visible_before_written")
 
 
+@pytest.mark.parametrize("stages", [1, 2, 5])
+def test_norm_variant_runs_clean(stages):
+    # with the RMSNorm the square warps also send their rows' Gram entries
+    # into the owners' records, after the same recv_free wait as the records
+    for seed in range(40):
+        simulate(ctas=4, tiles=8, stages_per_tile=stages, slots=3, lag=3, bufs=4, norm=True,
+                 seed=seed)
+    simulate(ctas=16, tiles=4, stages_per_tile=5, slots=3, lag=3, bufs=4, norm=True, seed=1)
+
+
+def test_gram_entries_sent_without_waiting_for_the_owner_are_caught():
+    assert _fails(ctas=4, tiles=6, stages_per_tile=2, slots=3, lag=3, bufs=4, norm=True,
+                  mutation="gram_without_recv_free")
+
+
 def test_full_cluster_of_sixteen():
     for seed in range(3):
         simulate(ctas=16, tiles=4, stages_per_tile=5, slots=3, lag=3, bufs=4, seed=seed)

@@ -12,6 +12,7 @@ import torch
 import oracle
 from oracle import compare
 from sinkhorn_mixing_gb300 import inputs
+from parity import bits, check_mixes_all, check_norm_all, check_split_all, oracle_mixes
 
 pytestmark = pytest.mark.gpu
 
@@ -169,3 +170,33 @@ def test_norm_rows_beyond_one_launch_grid(hc, d):
                                     np.random.default_rng(d).integers(0, n, 200)]))
     _, want = oracle.hc_rmsnorm(inputs.bf16_bits(yc[idx]), rw.cpu().numpy())
     assert key_diff(inputs.bf16_bits(y[idx]), want).max() <= 1
+
+
+def test_fused_norm_is_one_launch_and_matches_the_oracle_on_every_token(hc):
+    # 40,000 tokens at d = 5120 on the fused path: the RMSNorm is folded into
+    # the collapse (its statistic from the copies' Gram matrix), one launch;
+    # every token against the oracle, stage by stage
+    n, H, d = 40000, 4, 5120
+    x, w, sc, base, rw = case(n, H, d, 99)
+    before = hc.hc_launch_count()
+    y, pre, post, comb, m = hc.hc_mixes_pre_norm(x, w, sc, base, rw, 20, want_mixes=True)
+    torch.cuda.synchronize()
+    assert hc.hc_launch_count() - before == 1
+    xb = bits(x)
+    check_mixes_all(np64(m), oracle_mixes(None, xb, w.cpu().numpy(), 1e-20))
+    check_split_all(np64(m), np64(pre), np64(post), np64(comb), sc.cpu().numpy(),
+                    base.cpu().numpy(), H, 20, 1e-6)
+    check_norm_all(bits(y), xb, np64(pre), rw.cpu().numpy(), H,
+                   what="fused normalised y (40,000 tokens)")
+
+
+def test_fused_norm_coefficients_equal_the_plain_call(hc):
+    # the norm changes only y: mixes, pre, post and comb are bit for bit
+    # those of hc_mixes_pre (same squares, same order)
+    n, H, d = 3000, 4, 5120
+    x, w, sc, base, rw = case(n, H, d, 7)
+    y1, pre1, post1, comb1, m1 = hc.hc_mixes_pre_norm(x, w, sc, base, rw, 20, want_mixes=True)
+    y0, pre0, post0, comb0, m0 = hc.hc_mixes_pre(x, w, sc, base, 20, want_mixes=True)
+    torch.cuda.synchronize()
+    for a, b in ((pre1, pre0), (post1, post0), (comb1, comb0), (m1, m0)):
+        assert torch.equal(a, b)
