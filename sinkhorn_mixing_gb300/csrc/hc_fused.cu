@@ -612,29 +612,26 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                     // entries of the piece's four copies
 #pragma unroll
                     for (int m = 0; m < PP; ++m) {
-                        uint32_t wv[4][4];
+                        uint64_t xp[4][4];  // the piece's four copies, packed binary32 pairs
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint4 v = lds128(piece(j, m));
-                            wv[j][0] = v.x, wv[j][1] = v.y, wv[j][2] = v.z, wv[j][3] = v.w;
+                            xp[j][0] = bf16x2_to_f32x2(v.x);
+                            xp[j][1] = bf16x2_to_f32x2(v.y);
+                            xp[j][2] = bf16x2_to_f32x2(v.z);
+                            xp[j][3] = bf16x2_to_f32x2(v.w);
                         }
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const uint64_t xp = bf16x2_to_f32x2(wv[j][e]);
-                                ffma2(s2[m / 2][e], xp, xp);
-                            }
+                            for (int e = 0; e < 4; ++e) ffma2(s2[m / 2][e], xp[j][e], xp[j][e]);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            uint64_t xp[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) xp[j] = bf16x2_to_f32x2(wv[j][e]);
                             int q2 = 0;
 #pragma unroll
                             for (int j = 0; j < 4; ++j)
 #pragma unroll
-                                for (int k = j; k < 4; ++k) ffma2(g2[q2++], xp[j], xp[k]);
+                                for (int k = j; k < 4; ++k) ffma2(g2[q2++], xp[j][e], xp[k][e]);
                         }
                     }
                     __syncwarp();
@@ -708,6 +705,15 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
             }
 #pragma unroll
             for (int sh = 1; sh < LP; sh <<= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, sh);
+            // NORM: the row's Gram entries (the same in every lane of the row)
+            float gs[NORM ? kGram : 1];
+#pragma unroll
+            for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) {
+                gs[q2] = NORM ? sum2(g2[q2]) : 0.f;
+#pragma unroll
+                for (int sh = 1; sh < LP; sh <<= 1)
+                    if (NORM) gs[q2] += __shfl_xor_sync(0xFFFFFFFFu, gs[q2], sh);
+            }
             if (!__all_sync(0xFFFFFFFFu,
                             wait_bar<false>(bar(bSqEmpty(b)), (use & 1) ^ 1, abort, p.err)))
                 break;
@@ -718,14 +724,6 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 // the row's Gram entries go straight into its owner's record
                 // (floats 25..34), once the owner has read the previous
                 // tile's records; their bytes complete its recv_full
-                float gs[kGram];
-#pragma unroll
-                for (int q2 = 0; q2 < kGram; ++q2) {
-                    gs[q2] = sum2(g2[q2]);
-#pragma unroll
-                    for (int sh = 1; sh < LP; sh <<= 1)
-                        gs[q2] += __shfl_xor_sync(0xFFFFFFFFu, gs[q2], sh);
-                }
                 if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(kRecvFree), ((uint32_t)it & 1) ^ 1,
                                                             abort, p.err)))
                     break;
@@ -734,11 +732,12 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                     const uint32_t rec =
                         mapa(su32(sm.recv + (rank * kOwn + u) * kRec), (uint32_t)owner);
                     const uint32_t rfull = mapa(bar(kRecvFull), (uint32_t)owner);
+                    constexpr int g = NORM ? kGram : 1;  // (indices valid for NORM)
                     st_async_f32(rec + 100, gs[0], rfull);
-                    st_async_v2(rec + 104, gs[1], gs[2], rfull);
-                    st_async_v4(rec + 112, gs[3], gs[4], gs[5], gs[6], rfull);
-                    st_async_v2(rec + 128, gs[7], gs[8], rfull);
-                    st_async_f32(rec + 136, gs[9], rfull);
+                    st_async_v2(rec + 104, gs[1 % g], gs[2 % g], rfull);
+                    st_async_v4(rec + 112, gs[3 % g], gs[4 % g], gs[5 % g], gs[6 % g], rfull);
+                    st_async_v2(rec + 128, gs[7 % g], gs[8 % g], rfull);
+                    st_async_f32(rec + 136, gs[9 % g], rfull);
                 }
             }
         }
@@ -786,12 +785,16 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
         }
     } else if (warp == kWarpOwner) {
-        // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: lanes u < kOwn
-        // reduce the 16 records of their token in a fixed order, form r, m and
-        // pre for this CTA's collapse; lanes 16..31 then hand the record buffer
-        // back to the 16 senders, and lanes u < kOwn run the Sinkhorn for comb.
+        // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: the 8 lanes
+        // 8u..8u+7 reduce the 16 records of token u (lane 8u+q the records of
+        // senders q and q+8, then a butterfly over the 8 lanes: a fixed
+        // order), lane 8u forms r, m and pre for this CTA's collapse; lanes
+        // 16..31 then hand the record buffer back to the 16 senders, and
+        // lanes 8u run the Sinkhorn for comb.
+        const int u = lane >> 3;
+        const bool lead = (lane & 7) == 0;
         float bse[kMix], s0 = 0.f, s1 = 0.f, s2 = 0.f;
-        if (!mixes_only && lane < kOwn) {
+        if (!mixes_only && lead) {
 #pragma unroll
             for (int k = 0; k < kMix; ++k) bse[k] = __ldg(p.base + k);
             s0 = __ldg(p.scale + 0);
@@ -808,38 +811,48 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
             float G[NORM ? kGram : 1];  // NORM: the token's Gram entries over all d
 #pragma unroll
             for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) G[q2] = 0.f;
-            if (lane < kOwn) {
+            {
+                static_assert(kCluster == 16 && kOwn * 8 == 32, "8 lanes per owned token");
+                const float4 *ra = reinterpret_cast<const float4 *>(
+                    sm.recv + ((lane & 7) * kOwn + u) * kRec);
+                const float4 *rb = reinterpret_cast<const float4 *>(
+                    sm.recv + (((lane & 7) + 8) * kOwn + u) * kRec);
 #pragma unroll
-                for (int k = 0; k < kMix; ++k) m[k] = 0.f;
-                for (int src = 0; src < kCluster; ++src) {
-                    const float4 *r4 = reinterpret_cast<const float4 *>(
-                        sm.recv + (src * kOwn + lane) * kRec);
+                for (int v = 0; v < 6; ++v) {
+                    const float4 a4 = ra[v], b4 = rb[v];
+                    m[4 * v] = a4.x + b4.x;
+                    m[4 * v + 1] = a4.y + b4.y;
+                    m[4 * v + 2] = a4.z + b4.z;
+                    m[4 * v + 3] = a4.w + b4.w;
+                }
+                const float4 a6 = ra[6], b6 = rb[6];
+                ssum = a6.x + b6.x;
+                if (NORM) {
+                    const float4 a7 = ra[7], b7 = rb[7], a8 = ra[8], b8 = rb[8];
+                    const float ga[kGram] = {a6.y, a6.z, a6.w, a7.x, a7.y, a7.z, a7.w, a8.x, a8.y, a8.z};
+                    const float gb[kGram] = {b6.y, b6.z, b6.w, b7.x, b7.y, b7.z, b7.w, b8.x, b8.y, b8.z};
 #pragma unroll
-                    for (int v = 0; v < 6; ++v) {
-                        const float4 t4 = r4[v];
-                        m[4 * v] += t4.x;
-                        m[4 * v + 1] += t4.y;
-                        m[4 * v + 2] += t4.z;
-                        m[4 * v + 3] += t4.w;
-                    }
-                    const float4 t6 = r4[6];
-                    ssum += t6.x;
+                    for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) G[q2] = ga[q2] + gb[q2];
+                }
+#pragma unroll
+                for (int sh = 1; sh < 8; sh <<= 1) {
+#pragma unroll
+                    for (int k = 0; k < kMix; ++k) m[k] += __shfl_xor_sync(0xFFFFFFFFu, m[k], sh);
+                    ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, sh);
                     if (NORM) {
-                        const float4 t7 = r4[7], t8 = r4[8];
-                        const float gv[kGram] = {t6.y, t6.z, t6.w, t7.x, t7.y,
-                                                 t7.z, t7.w, t8.x, t8.y, t8.z};
 #pragma unroll
-                        for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2) G[q2] += gv[q2];
+                        for (int q2 = 0; q2 < (NORM ? kGram : 1); ++q2)
+                            G[q2] += __shfl_xor_sync(0xFFFFFFFFu, G[q2], sh);
                     }
                 }
             }
             float pr[4], po[4];
             int64_t t = 0;
-            if (lane < kOwn) {
+            if (lead) {
                 const float r = rsqrtf(ssum / p.F + p.norm_eps);
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) m[k] *= r;
-                t = (int64_t)tile * kTM + rank * kOwn + lane;
+                t = (int64_t)tile * kTM + rank * kOwn + u;
                 if (t < p.n && p.mixes != nullptr) {
                     float4 *dst = reinterpret_cast<float4 *>(p.mixes + t * kMix);
 #pragma unroll
@@ -869,7 +882,7 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                     // the collapse weights pre, and with NORM the token's
                     // RMSNorm factor
                     float4 *st4 =
-                        reinterpret_cast<float4 *>(sm.stage) + 2 * ((it % kColDoneBufs) * kOwn + lane);
+                        reinterpret_cast<float4 *>(sm.stage) + 2 * ((it % kColDoneBufs) * kOwn + u);
                     st4[0] = make_float4(pr[0], pr[1], pr[2], pr[3]);
                     if (NORM) st4[1] = make_float4(rs, 0.f, 0.f, 0.f);
                 }
@@ -886,7 +899,7 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 mbar_arrive_remote_relaxed(mapa(bar(kRecvFree), (uint32_t)(lane - (32 - kCluster))));
             if (!mixes_only) {
                 // then the Sinkhorn for comb, off the collapse's critical path
-                if (lane < kOwn) {
+                if (lead) {
                     float Cm[4][4];
                     sinkhorn_comb<4>([&](int k) { return m[k]; }, [&](int k) { return bse[k]; },
                                      s2, p.iters, p.eps, Cm);
