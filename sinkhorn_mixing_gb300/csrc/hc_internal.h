@@ -82,11 +82,6 @@ cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, con
                             const float *g, float eps, uint16_t *y, const DeviceInfo &di,
                             cudaStream_t s);
 
-// RMSNorm of bf16 rows [n][d] in place (d <= 8192), one row per CTA at a
-// time (rows beyond 2^20 taken in a grid stride).
-cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
-                           const DeviceInfo &di, cudaStream_t s);
-
 cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
                         const uint16_t *res, const float *post, const float *comb, uint16_t *y,
                         const DeviceInfo &di, cudaStream_t s);

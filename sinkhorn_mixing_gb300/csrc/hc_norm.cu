@@ -5,10 +5,10 @@
 // collapse, the mean of squares in fp32.
 //
 //   k_pre_norm       the collapse followed by the RMSNorm, one CTA per token
-//   k_rmsnorm        the RMSNorm alone, in place, after the fused kernel
 //
-// Both reduce the squares in a fixed order, so repeated calls give the same
-// bits.  (The decode kernel applies the same norm inside its own launch.)
+// It reduces the squares in a fixed order, so repeated calls give the same
+// bits.  (The decode and fused kernels apply the norm inside their own
+// launches.)
 #include "hc_common.cuh"
 #include "hc_internal.h"
 
@@ -84,57 +84,6 @@ __global__ void __launch_bounds__(256) k_pre_norm(int64_t n, int64_t nv, float e
     }
 }
 
-// --------------------------------------------------------- k_rmsnorm
-// RMSNorm of bf16 rows in place, one row per CTA at a time: each thread keeps
-// its vectors in registers while the mean of squares is reduced in a fixed
-// order, then writes (y * r) * g over them.
-__global__ void __launch_bounds__(256) k_rmsnorm(int64_t n, int64_t nv, float eps,
-                                                 uint4 *__restrict__ y,
-                                                 const float *__restrict__ g) {
-    constexpr int kPer = 4;  // vectors per thread held in registers (nv <= 1024)
-    __shared__ float red[8];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
-        uint4 *yt = y + t * nv;
-        uint4 v[kPer];
-        float ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int64_t q = threadIdx.x + (int64_t)k * 256;
-            if (q < nv) {
-                v[k] = yt[q];
-                float f[8];
-                unpack8(v[k], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-        if (lane == 0) red[warp] = ss;
-        __syncthreads();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) tot += red[w];
-        const float r = rsqrtf(tot / (float)(nv * 8) + eps);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int64_t q = threadIdx.x + (int64_t)k * 256;
-            if (q < nv) {
-                float f[8], o[8];
-                unpack8(v[k], f);
-                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q);
-                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(g) + 2 * q + 1);
-                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = (f[e] * r) * gv[e];
-                st_stream(yt + q, pack8(o));
-            }
-        }
-        __syncthreads();  // red[] is reused by the next row
-    }
-}
-
 // rows per launch grid: one CTA per row up to this many rows, then a stride
 constexpr int64_t kMaxRowGrid = int64_t(1) << 20;
 // collapsed rows up to this size stay in shared memory (two CTAs per SM)
@@ -169,14 +118,6 @@ cudaError_t launch_pre_norm(int64_t n, int hc, int64_t d, const uint16_t *x, con
         k_pre_norm<4, true><<<grid, 256, row, s>>>(n, nv, eps, xv, pre, g, yv);
     else
         k_pre_norm<8, true><<<grid, 256, row, s>>>(n, nv, eps, xv, pre, g, yv);
-    return launched();
-}
-
-cudaError_t launch_rmsnorm(int64_t n, int64_t d, uint16_t *y, const float *g, float eps,
-                           const DeviceInfo &, cudaStream_t s) {
-    if (d / 8 > 4 * 256) return cudaErrorNotSupported;
-    const unsigned grid = (unsigned)(n < kMaxRowGrid ? n : kMaxRowGrid);
-    k_rmsnorm<<<grid, 256, 0, s>>>(n, d / 8, eps, reinterpret_cast<uint4 *>(y), g);
     return launched();
 }
 
