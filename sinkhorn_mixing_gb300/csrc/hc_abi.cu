@@ -41,6 +41,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+bool overlap_launches() {
+    const char *e = getenv("HCMIX_PDL");
+    return e == nullptr || strcmp(e, "0") != 0;
+}
+
 ForcedPath forced_path() {
     const char *e = getenv("HCMIX_PATH");
     if (e == nullptr) return kPathAuto;

@@ -16,6 +16,15 @@ namespace hc {
 constexpr unsigned int kErrWaitTimeout = 1u;
 constexpr unsigned int kErrSmemLayout = 2u;  // shared memory base off its 1024-byte boundary
 
+// Programmatic dependent launch (see overlap_launches): wait until the
+// kernel before this one on the stream has completed and its memory is
+// visible (a no-op when this kernel was launched without the attribute),
+// then let the kernel after this one start launching.
+__device__ __forceinline__ void griddep_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- bf16
 
 // Two bf16 values packed in a 32-bit word -> two floats (exact).

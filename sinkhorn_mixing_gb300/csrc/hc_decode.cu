@@ -114,6 +114,7 @@ __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
+    griddep_wait_then_release();
     const int w = p.w, nf = 4 * w;
     const size_t wreg = wreg_bytes(w);
     float *ws = reinterpret_cast<float *>(smem);    // [24][nf]
@@ -458,13 +459,16 @@ cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, fl
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes(p.w, p.tpc);
     cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = kCluster;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    // 16-CTA clusters, with programmatic dependent launch (overlap_launches)
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap_launches() ? 2 : 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode, p);
     if (e != cudaSuccess) return e;
     return launched();

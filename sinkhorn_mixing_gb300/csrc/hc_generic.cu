@@ -193,6 +193,7 @@ template <int HC, int U>
 __global__ void __launch_bounds__(256) k_post(int64_t n, Units un, const uint4 *__restrict__ out,
                                               const uint4 *res, const float *__restrict__ post,
                                               const float *__restrict__ comb, uint4 *y) {
+    griddep_wait_then_release();
     const int lane = threadIdx.x & 31;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -268,6 +269,7 @@ __global__ void __launch_bounds__(256, 2) k_post_shared(int64_t n, Units un,
                                                          const float *__restrict__ post,
                                                          const float *__restrict__ comb, uint4 *y) {
     __shared__ float coef[8][HC * HC + HC];  // per warp: comb [j][k], then post [k]
+    griddep_wait_then_release();
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -379,10 +381,20 @@ cudaError_t launch_post(int64_t n, int hc, int64_t d, const uint16_t *out,
     const uint4 *ov = reinterpret_cast<const uint4 *>(out);
     const uint4 *rv = reinterpret_cast<const uint4 *>(res);
     uint4 *yv = reinterpret_cast<uint4 *>(y);
-    if (hc == 4)
-        k_post<4, 2><<<grid, 256, 0, s>>>(n, un, ov, rv, post, comb, yv);
-    else
-        k_post_shared<8><<<grid, 256, 0, s>>>(n, un, ov, rv, post, comb, yv);
+    // with programmatic dependent launch (overlap_launches)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = overlap_launches() ? 1 : 0;
+    const cudaError_t e =
+        hc == 4 ? cudaLaunchKernelEx(&cfg, k_post<4, 2>, n, un, ov, rv, post, comb, yv)
+                : cudaLaunchKernelEx(&cfg, k_post_shared<8>, n, un, ov, rv, post, comb, yv);
+    if (e != cudaSuccess) return e;
     return launched();
 }
 

@@ -35,6 +35,16 @@ cudaError_t device_info(DeviceInfo *out);
 enum ForcedPath { kPathAuto = 0, kPathGeneral = 1, kPathFused = 2, kPathFfma = 3 };
 ForcedPath forced_path();
 
+// Programmatic dependent launch for the small-batch kernels (k_decode,
+// k_post): launched with the programmatic-stream-serialization attribute,
+// such a kernel may start while the kernel before it on the stream is still
+// running; its first instruction waits (griddepcontrol.wait) until that
+// kernel has completed and its memory is visible, so no input is read early,
+// and it then lets the kernel after it start (launch_dependents).  What
+// overlaps is the launch and scheduling of one kernel with the tail of the
+// other.  HCMIX_PDL=0 in the environment turns it off (read at each call).
+bool overlap_launches();
+
 // The driver's cuTensorMapEncodeTiled, or nullptr when it is unavailable.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

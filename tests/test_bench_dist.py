@@ -90,8 +90,16 @@ def test_traffic_record_only_for_its_workload_and_source(tmp_path, monkeypatch):
     # the committed DRAM traffic belongs to the large hc=4 workload and to the
     # kernel source it was captured on; any other workload or an edited
     # source reports no traffic
-    rec = bench.traffic_record("hc_post", 4, 5120, 65536)
-    assert rec is not None and rec["dram_bytes_per_launch"] > 0
+    import hashlib
+    import json
+    committed = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for kernel in ("hc_mixes_pre", "hc_post"):
+        c = committed[kernel]
+        current = hashlib.sha256(open(os.path.join(ROOT, c["source"]), "rb").read()).hexdigest()[:16]
+        rec = bench.traffic_record(kernel, 4, 5120, 65536)
+        assert (rec is not None) == (current == c["source_sha256_16"])
+        if rec is not None:
+            assert rec["dram_bytes_per_launch"] > 0
     assert bench.traffic_record("hc_post", 8, 5120, 65536) is None
     assert bench.traffic_record("hc_mixes_pre", 4, 5120, 16384) is None
     assert bench.traffic_record("hc_mixes_pre", 4, 2048, 65536) is None
@@ -99,6 +107,12 @@ def test_traffic_record_only_for_its_workload_and_source(tmp_path, monkeypatch):
     src.write_text("a")
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"hc_post": dict(
-        rec, source="k.cu")}))
+        committed["hc_post"], source="k.cu")}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.traffic_record("hc_post", 4, 5120, 65536) is None
+    # the same record with the source's own hash is reported
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"hc_post": dict(
+        committed["hc_post"], source="k.cu",
+        source_sha256_16=hashlib.sha256(b"a").hexdigest()[:16])}))
+    rec = bench.traffic_record("hc_post", 4, 5120, 65536)
+    assert rec is not None and rec["dram_bytes_per_launch"] > 0

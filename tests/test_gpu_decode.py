@@ -184,3 +184,50 @@ def test_decode_under_cuda_graph_replay(hc):
     torch.cuda.synchronize()
     for a, b in zip((y, pre, post, comb, m), ref):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_chained_sublayers_equal_with_and_without_launch_overlap(hc, graph):
+    # Each kernel of the chain reads what the one before it wrote (x -> pre,
+    # post, comb -> the new x -> ...).  With programmatic dependent launch a
+    # kernel may start while its predecessor runs; it must still read only
+    # after it, so the chain ends on the same bits as with the launches
+    # serialised (HCMIX_PDL=0), eagerly and replayed from a CUDA graph.
+    n, d = 64, 5120
+    x0, w, sc, base = case(n, d, 31)
+    g = torch.Generator(device="cuda").manual_seed(32)
+    outs = [torch.randn((n, d), device="cuda", generator=g).to(torch.bfloat16) for _ in range(6)]
+
+    def chain(x):
+        for out in outs:
+            y, pre, post, comb, _ = hc.hc_mixes_pre(x, w, sc, base)
+            x = hc.hc_post(out + y, x, post, comb)
+        return x
+
+    results = []
+    for flag in ("1", "0"):
+        old = os.environ.get("HCMIX_PDL")
+        os.environ["HCMIX_PDL"] = flag
+        try:
+            if graph:
+                xs = x0.clone()
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    chain(xs)  # warm-up outside the capture
+                    torch.cuda.synchronize()
+                    gr = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gr, stream=side):
+                        xr = chain(xs)
+                    gr.replay()
+                torch.cuda.synchronize()
+                results.append(xr.clone())
+            else:
+                results.append(chain(x0.clone()))
+                torch.cuda.synchronize()
+        finally:
+            if old is None:
+                os.environ.pop("HCMIX_PDL", None)
+            else:
+                os.environ["HCMIX_PDL"] = old
+    assert torch.equal(results[0].view(torch.int16), results[1].view(torch.int16))
