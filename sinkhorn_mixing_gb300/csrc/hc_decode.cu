@@ -21,8 +21,10 @@
 //     squares) to the token's owner, CTA t of the cluster for its token t,
 //     with asynchronous 4-byte stores whose bytes complete the owner's
 //     barrier.  The owner sums the 16 records in CTA order, forms r, m and
-//     pre, sends pre to all 16 CTAs the same way and then runs the Sinkhorn
-//     for comb.
+//     pre and sends pre to all 16 CTAs the same way; beside it, warp 15 of
+//     the owner CTA (one the collapse of up to 14 tokens leaves idle) runs
+//     the Sinkhorn for comb from the mix numbers the owner left in shared
+//     memory.
 //   * Every CTA collapses its own w channels of the cluster's tokens from the
 //     x slice it holds, so x is read from memory once.
 //
@@ -109,7 +111,7 @@ __host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
 }
 __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
     return wreg_bytes(w) + xreg_bytes(w, tpc) + kCluster * kRecStride * 4 + kMaxTok * 4 * 4 +
-           kCluster * kMaxTok * 4 + 3 * 8 + 16;
+           kCluster * kMaxTok * 4 + 32 * 4 + 4 * 8 + 16;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
@@ -123,8 +125,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     float *recv = reinterpret_cast<float *>(smem + wreg + xreg_bytes(w, p.tpc));  // [16][28]
     float *preb = recv + kCluster * kRecStride;     // [16][4]: pre of the cluster's tokens
     float *normp = preb + kMaxTok * 4;              // [16 senders][16 tokens]: partial sums of y^2
-    uint64_t *bars = reinterpret_cast<uint64_t *>(normp + kCluster * kMaxTok);
-    int *abort_word = reinterpret_cast<int *>(bars + 3);
+    float *msh = normp + kCluster * kMaxTok;        // [24 (+8)]: the owned token's mix numbers
+    uint64_t *bars = reinterpret_cast<uint64_t *>(msh + 32);
+    int *abort_word = reinterpret_cast<int *>(bars + 4);
     volatile int *abort = abort_word;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
@@ -132,17 +135,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     const int tv = (int)((int64_t)p.n - tok0 < p.tpc ? (int64_t)p.n - tok0 : p.tpc);
     const bool mixes_only = p.mixes_only != 0;
     const uint32_t bRecv = su32(bars), bPre = su32(bars + 1), bNorm = su32(bars + 2);
+    const uint32_t bMix = su32(bars + 3);  // msh holds the owned token's mix numbers
+    constexpr int kWarpComb = kWarps - 1;  // runs the owned token's Sinkhorn
     const bool norm = p.rms_w != nullptr && !mixes_only;
     const int64_t F = 4LL * p.d;
 
     // Each barrier completes once: recv when the 16 records of this CTA's
     // token are in (owners only), pre when pre of all tv tokens is in, norm
-    // (with the RMSNorm) when every CTA's partial sum of y^2 of every token is.
+    // (with the RMSNorm) when every CTA's partial sum of y^2 of every token is,
+    // mix when the owner has put its token's mix numbers in msh.
     if (threadIdx.x == 0) {
         *abort_word = 0;
         mbar_init(bRecv, 1);
         mbar_init(bPre, 1);
         mbar_init(bNorm, 1);
+        mbar_init(bMix, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         if (rank < tv) mbar_expect_tx(bRecv, kCluster * kRecVals * 4);
         if (!mixes_only) mbar_expect_tx(bPre, (uint32_t)tv * 16);
@@ -254,14 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             const int64_t t = tok0 + rank;
             if (p.mixes != nullptr && lane < kMix) p.mixes[t * kMix + lane] = m;
             if (!mixes_only) {
+                // the mix numbers to the Sinkhorn warp first, so that comb
+                // is computed beside the split and the pre broadcast
+                if (lane < kMix) msh[lane] = m;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bMix);
                 float mm[kMix], bse[kMix];
 #pragma unroll
                 for (int k = 0; k < kMix; ++k) {
                     mm[k] = __shfl_sync(0xFFFFFFFFu, m, k);
                     bse[k] = __ldg(p.base + k);
                 }
-                const float s0 = __ldg(p.scale + 0), s1 = __ldg(p.scale + 1),
-                            s2 = __ldg(p.scale + 2);
+                const float s0 = __ldg(p.scale + 0), s1 = __ldg(p.scale + 1);
                 float pr[4], po[4];
                 split_pre_post<4>([&](int k) { return mm[k]; }, [&](int k) { return bse[k]; },
                                   s0, s1, p.eps, pr, po);
@@ -269,24 +280,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
                 if (lane < kCluster)
                     st_async_v4(mapa(su32(preb + rank * 4), (uint32_t)lane), pr[0], pr[1], pr[2],
                                 pr[3], mapa(bPre, (uint32_t)lane));
-                // comb on one lane: spread over 16 lanes (one entry each,
-                // shuffle row and column sums) it measured slower, a shuffle
-                // costing more than the three other rows' steps it saves
                 if (lane == 0) {
-                    float Cm[4][4];
-                    sinkhorn_comb<4>([&](int k) { return mm[k]; },
-                                     [&](int k) { return bse[k]; }, s2, p.iters, p.eps, Cm);
                     reinterpret_cast<float4 *>(p.pre)[t] = make_float4(pr[0], pr[1], pr[2], pr[3]);
                     reinterpret_cast<float4 *>(p.post)[t] =
                         make_float4(po[0], po[1], po[2], po[3]);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
-                            make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
                 }
             }
         }
     } else if (!mixes_only && warp > 0) {
+        if (warp == kWarpComb && rank < tv) {
+            // comb of the owned token, on one lane (spread over 16 lanes, one
+            // entry each with shuffle row and column sums, it measured
+            // slower: a shuffle costs more than the other rows' steps it
+            // saves), beside the owner warp's split and pre broadcast; then
+            // this warp's share of the collapse as usual
+            if (__all_sync(0xFFFFFFFFu, wait_bar<false>(bMix, 0, abort, p.err)) && lane == 0) {
+                float Cm[4][4];
+                sinkhorn_comb<4>([&](int k) { return msh[k]; }, [&](int k) { return __ldg(p.base + k); },
+                                 __ldg(p.scale + 2), p.iters, p.eps, Cm);
+                const int64_t t = tok0 + rank;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    reinterpret_cast<float4 *>(p.comb)[t * 4 + jj] =
+                        make_float4(Cm[jj][0], Cm[jj][1], Cm[jj][2], Cm[jj][3]);
+            }
+            __syncwarp();
+        }
         // Collapse y = sum_j pre_j x_j of this CTA's channels, warps 1..15,
         // one token per warp at a time.  With the RMSNorm the rows are kept
         // in shared memory (bf16), the warp's partial sum of y^2 goes to every
