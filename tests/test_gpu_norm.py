@@ -51,7 +51,8 @@ def key_diff(a_bits, b_bits):
 
 
 @pytest.mark.parametrize("n,H,d", [(5, 4, 64), (64, 4, 5120), (37, 4, 2304), (300, 8, 1024),
-                                   (1000, 4, 5120), (129, 4, 1024)])
+                                   (1000, 4, 5120), (129, 4, 1024), (200, 4, 2048),
+                                   (500, 4, 3072), (333, 4, 4096)])
 def test_norm_matches_oracle(hc, n, H, d):
     x, w, sc, base, rw = case(n, H, d, 3 * n + d + H)
     y, pre, post, comb, m = hc.hc_mixes_pre_norm(x, w, sc, base, rw, 20, want_mixes=True)
