@@ -256,7 +256,41 @@ def decode_latency(hc, dev, reps=20, replays=10):
         b.record(side)
         torch.cuda.synchronize(dev)
         eager_us = a.elapsed_time(b) * 1e3 / (replays * reps)
+    # the sublayer boundary on the same tokens (hc_post of one sublayer and
+    # hc_mixes_pre of the next in one call), replayed the same way
+    x_next = torch.empty_like(x)
+
+    def boundary():
+        hc.hc_post_mixes_pre(out, x, post, comb, p["w"], p["hc_scale"], p["hc_base"],
+                             wl.iters[0], wl.eps, wl.norm_eps, x_next=x_next, pre=pre,
+                             post_next=post2, comb_next=comb2, y=y, workspace=wsp)
+    post2 = torch.empty_like(post)
+    comb2 = torch.empty_like(comb)
+    with torch.cuda.stream(side):
+        for _ in range(5):
+            boundary()
+        torch.cuda.synchronize(dev)
+        launches0 = hc.hc_launch_count()
+        boundary()
+        torch.cuda.synchronize(dev)
+        boundary_launches = hc.hc_launch_count() - launches0
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gb, stream=side):
+            for _ in range(reps):
+                boundary()
+        torch.cuda.synchronize(dev)
+        gb.replay()
+        torch.cuda.synchronize(dev)
+        a.record(side)
+        for _ in range(replays):
+            gb.replay()
+        b.record(side)
+        torch.cuda.synchronize(dev)
+        boundary_us = a.elapsed_time(b) * 1e3 / (replays * reps)
     return {"workload": DESCR["decode"], "us_per_step_graph": graph_us,
+            "boundary_us_per_call_graph": boundary_us, "boundary_launches": boundary_launches,
+            "boundary": "hc_post of one sublayer + hc_mixes_pre of the next in one call "
+                        "(hc_post_mixes_pre), per call",
             "us_per_step_eager": eager_us, "tokens_per_s_graph": n / graph_us * 1e6,
             "l2": "warm (inputs stay in L2 between steps)",
             "graph": "%d steps per captured graph, %d replays" % (reps, replays)}

@@ -182,11 +182,12 @@ hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
  * Each sublayer uses the coefficients computed from its own input stream.
  * Results equal those of hc_post followed by hc_mixes_pre: x_next bit for
  * bit; the rest up to binary32 rounding order (bit for bit where both calls
- * take the same projection kernel).  On the fused path (hc = 4, d a multiple
- * of 1024 up to 5120, more tokens than the decode kernel takes) it is one
- * kernel that reads the residual once: the new stream is computed in shared
- * memory, stored to x_next and projected from there, which saves re-reading
- * it from HBM.
+ * take the same projection kernel).  At hc = 4 it is one kernel that reads
+ * the residual once -- the new stream is computed in shared memory, stored to
+ * x_next and projected from there, which saves re-reading it from HBM -- on
+ * the fused path (d a multiple of 1024 up to 5120, more tokens than the
+ * decode kernel takes) and on the decode path (up to 16 tokens per 16-CTA
+ * cluster the device co-schedules, d a multiple of 256 up to 5120).
  *   out [n, d] bf16;  residual [n, hc, d] bf16;  post [n, hc], comb [n, hc, hc]
  *   float -- sublayer s's output and coefficients (in)
  *   x_next [n, hc, d] bf16 (out) -- the new stream; x_next == residual (in

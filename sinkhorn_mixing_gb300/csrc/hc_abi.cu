@@ -461,7 +461,14 @@ hc_status hc_post_mixes_pre(int64_t n, int hc, int64_t d, const uint16_t *out,
                                                mixes, pre_next, post_next, comb_next, y_next, di,
                                                s));
     }
-    // other shapes and few tokens: hc_post, then hc_mixes_pre on its result.
+    if (hc::decode_supported(n, hc, d, di)) {
+        // few tokens: the decode kernel forms the new stream from the
+        // residual and output slices it loads, writes it, and goes on
+        return from_cuda(hc::launch_decode_post(n, hc, d, out, residual, post, comb, x_next, iters,
+                                                eps, norm_eps, w_mix, hc_scale, hc_base, mixes,
+                                                pre_next, post_next, comb_next, y_next, di, s));
+    }
+    // other shapes: hc_post, then hc_mixes_pre on its result.
     // hc_mixes_pre's workspace rule is checked here, before the first launch:
     // its general path keeps the mix numbers in the workspace.
     if (mixes == nullptr && !hc::decode_supported(n, hc, d, di) &&

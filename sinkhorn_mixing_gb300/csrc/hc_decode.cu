@@ -78,6 +78,13 @@ struct DecodeParams {
     unsigned int *err;
     const float *rms_w;  // RMSNorm weight of the sublayer input, or null
     float rms_eps;
+    // hc_post of the previous sublayer in front (null out: none): x is its
+    // residual stream, and the kernel works on x_next = hc_post(out, x,
+    // post_in, comb_in), which it also writes (x_next may be x itself)
+    const uint16_t *out;
+    const float *post_in;
+    const float *comb_in;
+    uint16_t *x_next;
 };
 
 __host__ __device__ constexpr int round4(int t) { return (t + 3) & ~3; }
@@ -92,6 +99,7 @@ __device__ __forceinline__ void cp_async_commit() {
 // Wait until at most `left` of this thread's copy groups are still pending.
 __device__ __forceinline__ void cp_async_wait(int left) {
     switch (left) {
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
         case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
         case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
         case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
@@ -109,8 +117,13 @@ __host__ __device__ constexpr size_t wreg_bytes(int w) {
 __host__ __device__ constexpr size_t xreg_bytes(int w, int tpc) {
     return (size_t)round4(tpc) * 4 * w * 2;
 }
+// the previous sublayer's output slice [round4(tpc)][w] bf16 (with hc_post in front)
+__host__ __device__ constexpr size_t oreg_bytes(int w, int tpc) {
+    return (size_t)round4(tpc) * w * 2;
+}
 __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
-    return wreg_bytes(w) + xreg_bytes(w, tpc) + kCluster * kRecStride * 4 + kMaxTok * 4 * 4 +
+    return wreg_bytes(w) + xreg_bytes(w, tpc) + oreg_bytes(w, tpc) + kCluster * kRecStride * 4 +
+           kMaxTok * 4 * 4 +
            kCluster * kMaxTok * 4 + 32 * 4 + 4 * 8 + 16;
 }
 
@@ -122,7 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     float *ws = reinterpret_cast<float *>(smem);    // [24][nf]
     float *part = ws;                               // [16 warps][28][33], after the projection
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + wreg);  // [round4(tpc)][nf]
-    float *recv = reinterpret_cast<float *>(smem + wreg + xreg_bytes(w, p.tpc));  // [16][28]
+    uint16_t *osh = reinterpret_cast<uint16_t *>(smem + wreg + xreg_bytes(w, p.tpc));  // [tpc][w]
+    float *recv = reinterpret_cast<float *>(smem + wreg + xreg_bytes(w, p.tpc) +
+                                            oreg_bytes(w, p.tpc));  // [16][28]
     float *preb = recv + kCluster * kRecStride;     // [16][4]: pre of the cluster's tokens
     float *normp = preb + kMaxTok * 4;              // [16 senders][16 tokens]: partial sums of y^2
     float *msh = normp + kCluster * kMaxTok;        // [24 (+8)]: the owned token's mix numbers
@@ -162,7 +177,75 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     // group per copy j, so that the projection of copy j starts as soon as
     // its group is in.  Rows up to the next multiple of 4 tokens are zero.
     // Rows by warp, 16-byte pieces by lane: no division in the index math.
-    {
+    const bool post_in_front = p.out != nullptr;
+    if (post_in_front) {
+        // With hc_post in front the new stream needs all four copies of a
+        // channel at once: group 0 takes the residual slice (all copies) and
+        // the output slice, groups 1..4 the W slice of copy j, so that the
+        // new stream is formed while W lands and the projection of copy j
+        // still starts as soon as its W is in.
+        const int wv = w / 4, xv = w / 8, tz = round4(tv);
+        for (int e = warp; e < 5 * tz; e += kWarps) {
+            const int t = e / 5, j = e % 5;  // j < 4: copy j of the residual; 4: out
+            uint16_t *dst = j < 4 ? xs + t * nf + j * w : osh + t * w;
+            if (t < tv) {
+                const uint16_t *src = j < 4 ? p.x + ((tok0 + t) * 4 + j) * (int64_t)p.d + rank * w
+                                            : p.out + (tok0 + t) * (int64_t)p.d + rank * w;
+                for (int q = lane; q < xv; q += 32) cp_async16(su32(dst + 8 * q), src + 8 * q);
+            } else {
+                for (int q = lane; q < xv; q += 32)
+                    *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        cp_async_commit();
+        for (int j = 0; j < 4; ++j) {
+            for (int i = warp; i < kMix; i += kWarps) {
+                const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
+                const uint32_t dst = su32(ws + i * nf + j * w);
+                for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
+            }
+            cp_async_commit();
+        }
+        cp_async_wait(4);
+        __syncthreads();  // the residual and output slices are in
+        // hc_post ("Mix projection" page, Block.hc_post), in the order of
+        // k_post: x'_k = post_k out + sum_i comb[i][k] x_i, rounded to bf16,
+        // written over the residual in shared memory (all four copies of a
+        // vector are read before any is written) and to x_next
+        for (int e = threadIdx.x; e < tv * xv; e += kThreads) {
+            const int t = e / xv, v = e % xv;
+            const int64_t tok = tok0 + t;
+            float po[4], cm[4][4];
+            const float4 pv = __ldg(reinterpret_cast<const float4 *>(p.post_in) + tok);
+            po[0] = pv.x, po[1] = pv.y, po[2] = pv.z, po[3] = pv.w;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 cv = __ldg(reinterpret_cast<const float4 *>(p.comb_in) + tok * 4 + i);
+                cm[i][0] = cv.x, cm[i][1] = cv.y, cm[i][2] = cv.z, cm[i][3] = cv.w;
+            }
+            float of[8], rf[4][8];
+            unpack8(*reinterpret_cast<const uint4 *>(osh + t * w + 8 * v), of);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                unpack8(*reinterpret_cast<const uint4 *>(xs + t * nf + i * w + 8 * v), rf[i]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float acc[8];
+#pragma unroll
+                for (int e2 = 0; e2 < 8; ++e2) {
+                    float s2 = po[k] * of[e2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) s2 = fmaf(cm[i][k], rf[i][e2], s2);
+                    acc[e2] = s2;
+                }
+                const uint4 nv = pack8(acc);
+                *reinterpret_cast<uint4 *>(xs + t * nf + k * w + 8 * v) = nv;
+                st_stream(reinterpret_cast<uint4 *>(p.x_next + (tok * 4 + k) * (int64_t)p.d +
+                                                    rank * w + 8 * v),
+                          nv);
+            }
+        }
+    } else {
         const int wv = w / 4, xv = w / 8, tz = round4(tv);
         for (int j = 0; j < 4; ++j) {
             for (int i = warp; i < kMix; i += kWarps) {
@@ -197,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     }
     for (int j = 0; j < 4; ++j) {
         cp_async_wait(3 - j);
-        __syncthreads();  // every thread's copies of group j are in
+        __syncthreads();  // every thread's copies of group j (j + 1 with hc_post) are in
         if (!active) continue;
         // unrolled, so that the loads of several feature blocks are in
         // flight together (the loop is bound by shared-memory latency)
@@ -442,11 +525,14 @@ bool decode_supported(int64_t n, int hc, int64_t d, const DeviceInfo &di) {
     return st.ok && n <= (int64_t)kMaxTok * st.max_clusters;
 }
 
-cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
-                          const uint16_t *x, const float *w, const float *scale,
-                          const float *base, float *mixes, float *pre, float *post,
-                          float *comb, uint16_t *y, const float *rms_w, float rms_eps,
-                          const DeviceInfo &di, cudaStream_t s) {
+namespace {
+
+cudaError_t launch_decode_impl(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                               const uint16_t *x, const float *w, const float *scale,
+                               const float *base, float *mixes, float *pre, float *post,
+                               float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                               const uint16_t *out, const float *post_in, const float *comb_in,
+                               uint16_t *x_next, const DeviceInfo &di, cudaStream_t s) {
     const DevState &st = dec_state(di);
     if (!st.ok || hc != 4 || n < 1 || n > (int64_t)kMaxTok * st.max_clusters)
         return cudaErrorNotSupported;
@@ -472,6 +558,10 @@ cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, fl
     p.err = di.err_word;
     p.rms_w = rms_w;
     p.rms_eps = rms_eps;
+    p.out = out;
+    p.post_in = post_in;
+    p.comb_in = comb_in;
+    p.x_next = x_next;
     const int nclusters = (int)((n + p.tpc - 1) / p.tpc);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
@@ -491,6 +581,28 @@ cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, fl
     const cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode, p);
     if (e != cudaSuccess) return e;
     return launched();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(int64_t n, int hc, int64_t d, int iters, float eps, float norm_eps,
+                          const uint16_t *x, const float *w, const float *scale,
+                          const float *base, float *mixes, float *pre, float *post,
+                          float *comb, uint16_t *y, const float *rms_w, float rms_eps,
+                          const DeviceInfo &di, cudaStream_t s) {
+    return launch_decode_impl(n, hc, d, iters, eps, norm_eps, x, w, scale, base, mixes, pre, post,
+                              comb, y, rms_w, rms_eps, nullptr, nullptr, nullptr, nullptr, di, s);
+}
+
+cudaError_t launch_decode_post(int64_t n, int hc, int64_t d, const uint16_t *out,
+                               const uint16_t *residual, const float *post_in,
+                               const float *comb_in, uint16_t *x_next, int iters, float eps,
+                               float norm_eps, const float *w, const float *scale,
+                               const float *base, float *mixes, float *pre, float *post,
+                               float *comb, uint16_t *y, const DeviceInfo &di, cudaStream_t s) {
+    if (pre == nullptr) return cudaErrorNotSupported;
+    return launch_decode_impl(n, hc, d, iters, eps, norm_eps, residual, w, scale, base, mixes, pre,
+                              post, comb, y, nullptr, 0.f, out, post_in, comb_in, x_next, di, s);
 }
 
 }  // namespace hc

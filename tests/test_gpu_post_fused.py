@@ -76,7 +76,11 @@ def restore(old):
     (129, 4, 1024, None, True),
     (1000, 4, 3072, None, True),
     (70, 4, 2048, "fused", True),     # the fused kernel below the decode limit
-    (33, 4, 5120, None, False),       # hc_post, then the decode kernel
+    (33, 4, 5120, None, True),        # the decode kernel with hc_post in front
+    (1, 4, 5120, None, True),
+    (64, 4, 2048, None, True),
+    (112, 4, 5120, None, True),       # 16 tokens on each of 7 clusters
+    (37, 4, 2304, None, True),        # w = 144: a channel slice not a multiple of 64
     (300, 4, 136, None, False),       # hc_post, then the general path
     (150, 8, 1024, None, False),      # hc=8: hc_post, then the general path
 ])
@@ -98,8 +102,9 @@ def test_equals_hc_post_then_hc_mixes_pre(hc, n, H, d, path, fused):
         assert torch.equal(a, b), nm
 
 
-def test_in_place_and_without_mixes(hc):
-    out, res, post, comb, w, sc, base = case(777, 4, 5120, seed=5)
+@pytest.mark.parametrize("n", [777, 50])  # the fused kernel; the decode kernel
+def test_in_place_and_without_mixes(hc, n):
+    out, res, post, comb, w, sc, base = case(n, 4, 5120, seed=5)
     want = separate(hc, out, res.clone(), post, comb, w, sc, base)
     x_next, y, pre, post1, comb1, m = hc.hc_post_mixes_pre(out, res, post, comb, w, sc, base,
                                                            x_next=res)
@@ -163,3 +168,22 @@ def test_overlapping_buffers_are_rejected_before_any_launch(hc):
         buf[:64].copy_(res)
         hc.hc_post_mixes_pre(out, buf[:64], post, comb, w, sc, base, x_next=buf[1:65])
     assert hc.hc_launch_count() == before
+
+
+def test_decode_boundary_against_the_oracle(hc):
+    # the decode kernel with hc_post in front, 112 tokens (16 on each of 7
+    # clusters), stage parity on every token
+    n = 112
+    out, res, post, comb, w, sc, base = case(n, 4, 5120, seed=91)
+    before = hc.hc_launch_count()
+    x1, y, pre, post1, comb1, m = hc.hc_post_mixes_pre(out, res, post, comb, w, sc, base,
+                                                       want_mixes=True)
+    torch.cuda.synchronize()
+    assert hc.hc_launch_count() - before == 1
+    xb = bits(x1)
+    check_post_all(xb, bits(out), bits(res), np64(post), np64(comb), 4,
+                   "decode boundary x_next (112 tokens)")
+    check_mixes_all(np64(m), oracle_mixes(None, xb, w.cpu().numpy(), 1e-20))
+    check_split_all(np64(m), np64(pre), np64(post1), np64(comb1), sc.cpu().numpy(),
+                    base.cpu().numpy(), 4, 20, 1e-6)
+    check_pre_all(bits(y), xb, np64(pre), 4, "decode boundary y (112 tokens)")
