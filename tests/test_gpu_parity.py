@@ -334,3 +334,41 @@ def test_bounded_wait_reports_a_timeout_and_the_context_survives(hc):
     torch.cuda.synchronize()
     assert hc.hc_device_error(clear=True) == 0
     assert bool(torch.isfinite(y.float()).all())
+
+
+@pytest.mark.parametrize("n,d,path", [
+    (37, 5120, "decode kernel"),          # the decode kernel (with hc_post in front for the boundary)
+    (200, 2048, "fused kernel"),          # the fused kernel's norm and post variants
+    (333, 5120, "fused kernel, 5 chunks per CTA"),
+])
+def test_guard_bytes_untouched_norm_and_boundary(hc, n, d, path):
+    # hc_mixes_pre_norm and hc_post_mixes_pre write nothing outside their
+    # outputs either: 64 sentinel elements on each side of every output
+    H, mix, pad = 4, 24, 64
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = torch.randn((n, H, d), device="cuda", generator=g).to(torch.bfloat16)
+    out = torch.randn((n, d), device="cuda", generator=g).to(torch.bfloat16)
+    w = torch.randn((mix, H * d), device="cuda", generator=g) / (H * d) ** 0.5
+    scale = torch.ones(3, device="cuda")
+    base = torch.zeros(mix, device="cuda")
+    rw = torch.rand(d, device="cuda", generator=g) + 0.5
+    post_in = torch.rand((n, H), device="cuda", generator=g) * 2
+    comb_in = torch.rand((n, H, H), device="cuda", generator=g) / H
+
+    def padded(shape, dtype):
+        numel = int(np.prod(shape))
+        buf = torch.full((numel + 2 * pad,), 77, dtype=dtype, device="cuda")
+        return buf, buf[pad:pad + numel].view(shape)
+
+    bufs = [padded((n, mix), torch.float32), padded((n, H), torch.float32),
+            padded((n, H), torch.float32), padded((n, H, H), torch.float32),
+            padded((n, d), torch.bfloat16)]
+    (bm, m), (bp, pre), (bq, post), (bc, comb), (by, y) = bufs
+    hc.hc_mixes_pre_norm(x, w, scale, base, rw, mixes=m, pre=pre, post=post, comb=comb, y=y)
+    bx, xn = padded((n, H, d), torch.bfloat16)
+    bufs.append((bx, xn))
+    hc.hc_post_mixes_pre(out, x, post_in, comb_in, w, scale, base, x_next=xn, mixes=m, pre=pre,
+                         post_next=post, comb_next=comb, y=y)
+    torch.cuda.synchronize()
+    for buf, _ in bufs:
+        assert torch.all(buf[:pad] == 77) and torch.all(buf[-pad:] == 77), path
