@@ -408,10 +408,24 @@ def e2e_pipelined(hc, args, wl, x, out, p, iters, ws, dev, chunks=8):
     b.record(s_out)
     torch.cuda.synchronize(dev)
     te = max_over_ranks(a.elapsed_time(b) / 1e3, ws, dev)
+    # the host link as this machine gives it now: one chunk's x copied in and its
+    # stream result copied out, each alone (the bound the pipeline works
+    # against: the host is shared with other GPUs' jobs, and varies)
+    link = {}
+    for name, dst, src in (("h2d", slots[0]["x"], xh[:cs]), ("d2h", ysh[:cs], slots[0]["ys"])):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        a.record()
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(dev)
+        link[name + "_gbps"] = 3 * src.numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9
     return {"value": job_tokens_per_s(ws, n, args.e2e_steps, te), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
             "pipeline": "%d token chunks per step, copy-in / compute / copy-out streams"
-                        % len(bounds)}
+                        % len(bounds),
+            "host_link_measured": link}
 
 
 def _flush_buffer(in_bytes, dev):
