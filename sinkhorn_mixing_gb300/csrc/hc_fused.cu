@@ -36,6 +36,21 @@
 //   releases every stage in order, so each wait is for the phase right after
 //   one it has already seen.
 //
+// Two variants of the same kernel (template flags):
+//   * POST (hc_post_mixes_pre): hc_post of the previous sublayer in front.
+//     The ring streams the residual; 8 post warps (20 warps in all) rewrite
+//     each stage in place into the new stream (post_k out + sum_j comb[j][k]
+//     x_j, in hc_post's order), which the MMA and the squares then read; the
+//     MMA thread stores each rewritten stage to x_next with one TMA store
+//     from the slot and, at a tile's last stage, waits for the stores to
+//     complete before the tile's records may leave (the collapse re-reads
+//     x_next).
+//   * NORM (hc_mixes_pre_norm): the RMSNorm of the collapse.  The square
+//     warps also sum the ten entries G_jk = sum_c x_jc x_kc of each row's
+//     copies and store them into the owners' records; the owner forms the
+//     collapse's sum of squares as pre^T G pre, so its RMS factor is known
+//     before the collapse writes y = bf16((bf16(sum_j pre_j x_j) g) r).
+//
 // Every wait is bounded: a wait that exceeds kTimeoutNs sets the CTA's abort
 // flag and bit 0 of the device error word, and all roles then run to the
 // common teardown (no trap, TMEM always freed, no CTA leaves its cluster
