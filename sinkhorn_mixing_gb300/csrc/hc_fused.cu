@@ -105,20 +105,23 @@ constexpr int kWarpEpi0 = 8;     // 8, 9: TMEM read-out (lanes 0..63), records t
 constexpr int kWarpOwner = 12;   // reduces the records of this CTA's tokens, Sinkhorn
 constexpr int kCollapseWarps = 7;
 constexpr int kCollapseThreads = kCollapseWarps * 32;
-template <bool POST>
+// The wide layout (POST, and NORM whose square warps also sum the Gram
+// entries) has 20 warps and 8 square warps; the plain one 16 and 4.
+template <bool POST, bool NORM = false>
 struct Roles {
-    static constexpr int kWarps = POST ? 20 : 16;
+    static constexpr bool kWide = POST || NORM;
+    static constexpr int kWarps = kWide ? 20 : 16;
     static constexpr int kThreads = kWarps * 32;
     // square warps (with POST: post warps): 2..5, or 2..7, 10, 11
-    static constexpr int kSqWarps = POST ? 8 : 4;
+    static constexpr int kSqWarps = kWide ? 8 : 4;
     __host__ __device__ static constexpr int sq_index(int w) {
-        return (w >= 2 && w < (POST ? 8 : 6)) ? w - 2 : (POST && (w == 10 || w == 11)) ? w - 4 : -1;
+        return (w >= 2 && w < (kWide ? 8 : 6)) ? w - 2 : (kWide && (w == 10 || w == 11)) ? w - 4 : -1;
     }
     // collapse warps: 6, 7, 10, 11, 13, 14, 15, or 13..19
     __host__ __device__ static constexpr int col_index(int w) {
-        return POST ? (w >= 13 && w < 20 ? w - 13 : -1)
-                    : (w == 6 ? 0 : w == 7 ? 1 : w == 10 ? 2 : w == 11 ? 3
-                                                 : (w >= 13 && w < 16 ? w - 9 : -1));
+        return kWide ? (w >= 13 && w < 20 ? w - 13 : -1)
+                     : (w == 6 ? 0 : w == 7 ? 1 : w == 10 ? 2 : w == 11 ? 3
+                                                  : (w >= 13 && w < 16 ? w - 9 : -1));
     }
     // Ring consumers: the MMA commit and the square warps; with POST the MMA
     // commit and the MMA thread once the slot's TMA store has read it (the
@@ -131,11 +134,12 @@ struct Roles {
     static constexpr int kSqFullArrivals = kSqWarps + (POST ? 1 : 0);
     // lanes per token row in the square warps: a lane covers 8 / kLanesPerRow
     // 16-byte pieces (8 channels each) of each copy
-    static constexpr int kLanesPerRow = POST ? 4 : 2;
+    static constexpr int kLanesPerRow = kWide ? 4 : 2;
     static constexpr int kPieces = 8 / kLanesPerRow;
 };
 constexpr int kThreadsPlain = Roles<false>::kThreads;
-constexpr int kThreadsPost = Roles<true>::kThreads;
+constexpr int kThreadsWide = Roles<true>::kThreads;
+static_assert(Roles<false, true>::kThreads == kThreadsWide, "POST and NORM share a layout");
 
 // tcgen05 instruction descriptor: D f32, A/B bf16, both K-major, N=48, M=128.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kNW >> 3) << 17) |
@@ -288,10 +292,10 @@ __device__ __forceinline__ int chunk_feature(int kc, int rank, const FusedParams
 // NCC = w / 64 (64-channel sub-tiles per copy per CTA) is a template
 // parameter so that all index arithmetic is by constants.
 template <int NCC, bool POST, bool NORM>
-__global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<POST, NORM>::kThreads, 1)
     k_fused(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_xn,
             const __grid_constant__ CUtensorMap tmap_out, const FusedParams p) {
-    using R = Roles<POST>;
+    using R = Roles<POST, NORM>;
     constexpr int kThreads = R::kThreads;
     static_assert(!(POST && NORM), "hc_post in front and the RMSNorm behind are separate variants");
     constexpr uint32_t kRecvTx = recv_tx(NORM);
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
     // piece of W is read once for both rows, with kPieces pieces in flight
     // per thread (one piece at a time waited a full L2 round trip each).
     {
-        constexpr int kPieces = POST ? 4 : 8;  // 96 registers with POST
+        constexpr int kPieces = R::kWide ? 4 : 8;  // 96 registers in the wide layout
         const int nkc = 4 * ncc;
         const int total = kMix * nkc * 8;  // (piece q, row i, chunk kc)
         const int64_t F = 4LL * p.d;
@@ -941,22 +945,8 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
         constexpr int nv = NCC * 8 * kCluster;  // vectors per copy row (d / 8)
         constexpr int nout = kOwn * nv;
         const uint4 *x = reinterpret_cast<const uint4 *>(p.x);
-        // NORM: the RMSNorm weight of this thread's vectors v = ct + 224 k,
-        // held for the whole launch
+        // NORM: this thread's vectors v = ct + 224 k (8 channels each)
         constexpr int kNormV = NORM ? (nv + kCollapseThreads - 1) / kCollapseThreads : 1;
-        float gw[kNormV][8];
-#pragma unroll
-        for (int k = 0; k < kNormV; ++k) {
-            const int v = ct + k * kCollapseThreads;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) gw[k][e] = 0.f;
-            if (NORM && v < nv) {
-                const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v);
-                const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v + 1);
-                gw[k][0] = g0.x, gw[k][1] = g0.y, gw[k][2] = g0.z, gw[k][3] = g0.w;
-                gw[k][4] = g1.x, gw[k][5] = g1.y, gw[k][6] = g1.z, gw[k][7] = g1.w;
-            }
-        }
         for (int it = 0; it < T; ++it) {
             const int tile = cluster + it * nclusters;
             const int ib = it % kColDoneBufs;
@@ -966,49 +956,57 @@ __global__ void __launch_bounds__(Roles<POST>::kThreads, 1)
                 break;
             const int64_t tok0 = (int64_t)tile * kTM + rank * kOwn;
             if (NORM) {
-                // vector v (8 channels) of all kOwn tokens per step, so that
-                // the weight held for v serves the four of them:
+                // vector v (8 channels) of all kOwn tokens per step, two
+                // tokens' loads in flight at a time (96 registers), so that
+                // the weight loaded once for v serves the four of them:
                 // y = bf16((bf16(sum_j pre_j x_j) g) r)
 #pragma unroll
                 for (int k = 0; k < kNormV; ++k) {
                     const int v = ct + k * kCollapseThreads;
                     if (v >= nv) break;
-                    uint4 xv[kOwn][4];
+                    const float4 g0 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v);
+                    const float4 g1 = __ldg(reinterpret_cast<const float4 *>(p.rms_w) + 2 * v + 1);
+                    const float gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-                    for (int u = 0; u < kOwn; ++u) {
-                        const int64_t tok = tok0 + u;
-                        if (tok < p.n) {
+                    for (int h2 = 0; h2 < kOwn; h2 += 2) {
+                        uint4 xv[2][4];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) xv[u][j] = __ldcs(x + (tok * 4 + j) * nv + v);
+                        for (int u = 0; u < 2; ++u) {
+                            const int64_t tok = tok0 + h2 + u;
+                            if (tok < p.n) {
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    xv[u][j] = __ldcs(x + (tok * 4 + j) * nv + v);
+                            }
                         }
-                    }
 #pragma unroll
-                    for (int u = 0; u < kOwn; ++u) {
-                        const int64_t tok = tok0 + u;
-                        if (tok < p.n) {
-                            const float4 *st4 =
-                                reinterpret_cast<const float4 *>(sm.stage) + 2 * (ib * kOwn + u);
-                            const float4 pr = st4[0];
-                            const float rs = st4[1].x;
-                            float acc[8], f[8];
-                            unpack8(xv[u][0], f);
+                        for (int u = 0; u < 2; ++u) {
+                            const int64_t tok = tok0 + h2 + u;
+                            if (tok < p.n) {
+                                const float4 *st4 = reinterpret_cast<const float4 *>(sm.stage) +
+                                                    2 * (ib * kOwn + h2 + u);
+                                const float4 pr = st4[0];
+                                const float rs = st4[1].x;
+                                float acc[8], f[8];
+                                unpack8(xv[u][0], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
-                            unpack8(xv[u][1], f);
+                                for (int e = 0; e < 8; ++e) acc[e] = pr.x * f[e];
+                                unpack8(xv[u][1], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
-                            unpack8(xv[u][2], f);
+                                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.y, f[e], acc[e]);
+                                unpack8(xv[u][2], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
-                            unpack8(xv[u][3], f);
+                                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.z, f[e], acc[e]);
+                                unpack8(xv[u][3], f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
-                            // the collapse in bf16 (as hc_pre writes it), then
-                            // the RMSNorm: (y g) r
-                            unpack8(pack8(acc), f);
+                                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pr.w, f[e], acc[e]);
+                                // the collapse in bf16 (as hc_pre writes it),
+                                // then the RMSNorm: (y g) r
+                                unpack8(pack8(acc), f);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = (f[e] * gw[k][e]) * rs;
-                            st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + v, pack8(acc));
+                                for (int e = 0; e < 8; ++e) acc[e] = (f[e] * gw[e]) * rs;
+                                st_stream(reinterpret_cast<uint4 *>(p.y) + tok * nv + v, pack8(acc));
+                            }
                         }
                     }
                 }
@@ -1076,7 +1074,7 @@ struct DevState {
     bool init = false;
     unsigned long long ctx = 0;  // the context the set-up below was done in
     bool ok = false;
-    int max_clusters[2] = {0, 0};  // co-resident clusters, without / with POST
+    int max_clusters[2] = {0, 0};  // co-resident clusters, plain / wide layout
 };
 std::mutex g_fmu;
 DevState g_dev[64];
@@ -1125,7 +1123,7 @@ const DevState &dev_state(const DeviceInfo &di) {
     for (int post = 0; post < 2; ++post) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(kCluster);
-        cfg.blockDim = dim3(post ? kThreadsPost : kThreadsPlain);
+        cfg.blockDim = dim3(post ? kThreadsWide : kThreadsPlain);
         cfg.dynamicSmemBytes = smem_bytes(kMaxNcc);
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -1232,11 +1230,11 @@ cudaError_t launch_impl(int64_t n, int64_t d, int iters, float eps, float norm_e
     p.x_next = x_next;
     p.rms_w = rms_w;
     p.rms_eps = rms_eps;
-    const int mc = st.max_clusters[with_post ? 1 : 0];
+    const int mc = st.max_clusters[with_post || with_norm ? 1 : 0];
     const int nclusters = p.num_tiles < mc ? p.num_tiles : mc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(nclusters * kCluster));
-    cfg.blockDim = dim3(with_post ? kThreadsPost : kThreadsPlain);
+    cfg.blockDim = dim3(with_post || with_norm ? kThreadsWide : kThreadsPlain);
     cfg.dynamicSmemBytes = smem_bytes(p.ncc);
     cfg.stream = s;
     cudaLaunchAttribute attr;

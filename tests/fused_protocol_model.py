@@ -17,7 +17,8 @@ the kernel's roles as generators that yield the barrier waits they make:
             and releases it, and at a tile's last stage waits until the
             tile's stores are written and arrives on its sq_full first;
   sq (x4)   consume every stage in order, release it, publish the tile's sums
-            of squares through sq_full / sq_empty; with `post` (x8) they
+            of squares through sq_full / sq_empty (x8 with `norm`); with
+            `post` (x8) they
             first rewrite the stage in place (hc_post of the previous
             sublayer) and signal post_done, and leave the release to the MMA
             thread; with `norm` each also waits until the previous tile's
@@ -119,7 +120,7 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
         events.append(fn)
 
     C, T, NS, S = ctas, tiles, stages_per_tile, slots
-    NSQ = 8 if post else 4
+    NSQ = 8 if (post or norm) else 4  # the wide layout of both variants
     written = set()  # (rank, stage) of x_next stores that reached memory
     cs = []
     for r in range(C):
@@ -129,7 +130,7 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             post_done=[Barrier("post_done", NSQ) for _ in range(S)],
             posted=[set() for _ in range(S)],
             # MMA commit + 4 square warps; with post MMA commit + store read
-            empty=[Barrier("empty", 2 if post else 5) for _ in range(S)],
+            empty=[Barrier("empty", 2 if post else 1 + NSQ) for _ in range(S)],
             stores=[],
             slot=[None] * S, holders=[set() for _ in range(S)],
             acc_full=[Barrier("acc_full", 1) for _ in range(2)],
@@ -139,13 +140,20 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             sq_empty=[Barrier("sq_empty", 2) for _ in range(2)],
             sq=[[None] * NSQ, [None] * NSQ],
             recv_full=Barrier("recv_full", 1), recv_free=Barrier("recv_free", C),
-            recv=[None] * C, recv_g=[None] * C, reading=[False],
+            recv=[None] * C, recv_g={}, reading=[False],
             pre_ready=[Barrier("pre_ready", 1) for _ in range(bufs)],
             col_done=[Barrier("col_done", 2) for _ in range(bufs)],
             stage=[None] * bufs, stage_readers=[0] * bufs))
-    per_round = 2 * C if norm else C  # records (and Gram entries) per round
-    for c in cs:
-        c["recv_full"].expect_tx(per_round)
+    # with norm, square warp w holds the rows of tokens TW*w .. TW*w+TW-1 of
+    # the 64-token tile and sends each row's Gram entries to the row's owner
+    # (TO tokens per owner): every owner hears from every warp that holds one
+    # of its rows, in every CTA
+    TW, TO = 64 // NSQ, 64 // C
+    covers = [sorted({t // TO for t in range(TW * w, TW * w + TW)}) for w in range(NSQ)]
+    gram_from = [[w for w in range(NSQ) if o in covers[w]] for o in range(C)]
+    per_round = [C + (C * len(gram_from[o]) if norm else 0) for o in range(C)]
+    for r, c in enumerate(cs):
+        c["recv_full"].expect_tx(per_round[r])
 
     def producer(c):
         for it in range(T):
@@ -253,15 +261,14 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             if norm:
                 if mutation != "gram_without_recv_free":
                     yield wait(c["recv_free"], (it & 1) ^ 1)
-                lo, hi = w * C // NSQ, (w + 1) * C // NSQ
-                for o in range(lo, hi):
-                    def deliver_g(o=o, it=it, rank=c["rank"]):
+                for o in covers[w]:
+                    def deliver_g(o=o, it=it, rank=c["rank"], w=w):
                         oc = cs[o]
                         if oc["reading"][0]:
                             raise ProtocolError("Gram entries land while their owner reads")
-                        if oc["recv_g"][rank] is not None:
+                        if oc["recv_g"].get((rank, w)) is not None:
                             raise ProtocolError("Gram entries overwrite unread ones")
-                        oc["recv_g"][rank] = it
+                        oc["recv_g"][(rank, w)] = it
                         oc["recv_full"].complete_tx(1)
                     later(deliver_g)
 
@@ -300,7 +307,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
             yield wait(c["recv_full"], it & 1)
             if c["recv"] != [it] * C:
                 raise ProtocolError("owner of tile %d finds records %s" % (it, c["recv"]))
-            if norm and c["recv_g"] != [it] * C:
+            if norm and any(c["recv_g"].get((r, w)) != it for r in range(C)
+                            for w in gram_from[c["rank"]]):
                 raise ProtocolError("owner of tile %d finds Gram entries %s" % (it, c["recv_g"]))
             if mutation == "release_before_read":
                 for d in cs:
@@ -315,8 +323,8 @@ def simulate(ctas=4, tiles=5, stages_per_tile=5, slots=3, lag=3, bufs=4, mixes_o
                 c["stage"][i] = it
                 c["pre_ready"][i].arrive()
             c["recv"] = [None] * C
-            c["recv_g"] = [None] * C
-            c["recv_full"].expect_tx(per_round)
+            c["recv_g"] = {}
+            c["recv_full"].expect_tx(per_round[c["rank"]])
             if mutation != "release_before_read":
                 for d in cs:
                     later(lambda d=d: d["recv_free"].arrive())
