@@ -161,6 +161,12 @@ hc_status hc_mixes_pre(int64_t n, int hc, int64_t d, int iters, float eps,
  *   1e-20); all other arguments, the workspace rule included, as in
  *   hc_mixes_pre.  y holds the normalised rows; pre/post/comb/mixes are those
  *   of hc_mixes_pre.  rms_weight == NULL is HC_ERR_INVALID_ARG.
+ * One launch on every path.  On the fused path (hc = 4, d a multiple of 1024
+ * above the decode limit) the mean of squares is that of the binary32
+ * collapse before its bf16 rounding (pre^T G pre, G the copies' Gram matrix
+ * summed while the tokens stream through), so the factor is known before y
+ * is written; it differs from the formula above by far less than one bf16
+ * step of y.
  */
 hc_status hc_mixes_pre_norm(int64_t n, int hc, int64_t d, int iters, float eps,
                             float norm_eps, const uint16_t *x, const float *w_mix,
