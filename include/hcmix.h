@@ -33,6 +33,17 @@
  *   - The library never aborts, exits or traps.  CUDA launch failures are
  *     returned as HC_ERR_CUDA.  Kernels with bounded internal waits record a
  *     timeout in a per-device error word that hc_device_error() reads.
+ *   - Launch overlap (environment variable HCMIX_PDL=0 turns it off): the
+ *     decode kernel (hc = 4, d % 256 == 0, d <= 5120, up to 16 tokens per
+ *     16-CTA cluster the device co-schedules: 112 on GB300; it serves
+ *     hc_mixes, hc_mixes_pre, hc_mixes_pre_norm and hc_post_mixes_pre on
+ *     those shapes) and the hc_post kernel are launched with programmatic
+ *     dependent launch, so they may start while the kernel enqueued just
+ *     before them in the stream is still running.  They read every
+ *     activation only after that kernel has completed, but the decode kernel
+ *     starts copying its slice of w_mix at once: w_mix must not be written by
+ *     the kernel enqueued immediately before the call (weights written by an
+ *     earlier kernel, a copy or a memset in between are fine).
  */
 #ifndef HCMIX_H
 #define HCMIX_H

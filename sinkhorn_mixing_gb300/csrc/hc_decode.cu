@@ -129,10 +129,28 @@ __host__ __device__ constexpr size_t smem_bytes(int w, int tpc) {
 
 __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    griddep_wait_then_release();
     const int w = p.w, nf = 4 * w;
     const size_t wreg = wreg_bytes(w);
     float *ws = reinterpret_cast<float *>(smem);    // [24][nf]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)(blockIdx.x % kCluster);
+    const int64_t F = 4LL * p.d;
+    // The W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) first, one
+    // copy group per copy j, before the wait for the kernel in front: W_mix is
+    // a parameter, not an activation, so its copies overlap that kernel's tail
+    // (with programmatic dependent launch) and everything the kernel in front
+    // writes is read only after the wait.  Rows by warp, 16-byte pieces by
+    // lane: no division in the index math.
+    for (int j = 0; j < 4; ++j) {
+        const int wv = w / 4;
+        for (int i = warp; i < kMix; i += kWarps) {
+            const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
+            const uint32_t dst = su32(ws + i * nf + j * w);
+            for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
+        }
+        cp_async_commit();
+    }
+    griddep_wait_then_release();
     float *part = ws;                               // [16 warps][28][33], after the projection
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + wreg);  // [round4(tpc)][nf]
     uint16_t *osh = reinterpret_cast<uint16_t *>(smem + wreg + xreg_bytes(w, p.tpc));  // [tpc][w]
@@ -144,8 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     uint64_t *bars = reinterpret_cast<uint64_t *>(msh + 32);
     int *abort_word = reinterpret_cast<int *>(bars + 4);
     volatile int *abort = abort_word;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)(blockIdx.x % kCluster);
     const int64_t tok0 = (int64_t)(blockIdx.x / kCluster) * p.tpc;
     const int tv = (int)((int64_t)p.n - tok0 < p.tpc ? (int64_t)p.n - tok0 : p.tpc);
     const bool mixes_only = p.mixes_only != 0;
@@ -153,7 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     const uint32_t bMix = su32(bars + 3);  // msh holds the owned token's mix numbers
     constexpr int kWarpComb = kWarps - 1;  // runs the owned token's Sinkhorn
     const bool norm = p.rms_w != nullptr && !mixes_only;
-    const int64_t F = 4LL * p.d;
 
     // Each barrier completes once: recv when the 16 records of this CTA's
     // token are in (owners only), pre when pre of all tv tokens is in, norm
@@ -172,19 +187,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     }
     cluster_arrive();  // waited for before the first remote store
 
-    // W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) and x slice
-    // (token t, copy j -> x[tok0+t][j][r*w ...]) as asynchronous copies, one
-    // group per copy j, so that the projection of copy j starts as soon as
-    // its group is in.  Rows up to the next multiple of 4 tokens are zero.
-    // Rows by warp, 16-byte pieces by lane: no division in the index math.
+    // The x slice (token t, copy j -> x[tok0+t][j][r*w ...]) follows as
+    // asynchronous copies, one group per copy j after the four W groups, so
+    // that the projection of copy j starts as soon as its group is in.  Rows
+    // up to the next multiple of 4 tokens are zero.
     const bool post_in_front = p.out != nullptr;
     if (post_in_front) {
         // With hc_post in front the new stream needs all four copies of a
-        // channel at once: group 0 takes the residual slice (all copies) and
-        // the output slice, groups 1..4 the W slice of copy j, so that the
-        // new stream is formed while W lands and the projection of copy j
-        // still starts as soon as its W is in.
-        const int wv = w / 4, xv = w / 8, tz = round4(tv);
+        // channel at once: one group takes the residual slice (all copies)
+        // and the output slice.
+        const int xv = w / 8, tz = round4(tv);
         for (int e = warp; e < 5 * tz; e += kWarps) {
             const int t = e / 5, j = e % 5;  // j < 4: copy j of the residual; 4: out
             uint16_t *dst = j < 4 ? xs + t * nf + j * w : osh + t * w;
@@ -198,16 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             }
         }
         cp_async_commit();
-        for (int j = 0; j < 4; ++j) {
-            for (int i = warp; i < kMix; i += kWarps) {
-                const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
-                const uint32_t dst = su32(ws + i * nf + j * w);
-                for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
-            }
-            cp_async_commit();
-        }
-        cp_async_wait(4);
-        __syncthreads();  // the residual and output slices are in
+        cp_async_wait(0);
+        __syncthreads();  // the residual and output slices (and W) are in
         // hc_post ("Mix projection" page, Block.hc_post), in the order of
         // k_post: x'_k = post_k out + sum_i comb[i][k] x_i, rounded to bf16,
         // written over the residual in shared memory (all four copies of a
@@ -246,13 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             }
         }
     } else {
-        const int wv = w / 4, xv = w / 8, tz = round4(tv);
+        const int xv = w / 8, tz = round4(tv);
         for (int j = 0; j < 4; ++j) {
-            for (int i = warp; i < kMix; i += kWarps) {
-                const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
-                const uint32_t dst = su32(ws + i * nf + j * w);
-                for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
-            }
             for (int t = warp; t < tz; t += kWarps) {
                 uint16_t *dst = xs + t * nf + j * w;
                 if (t < tv) {
@@ -279,8 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         for (int k = 0; k < 6; ++k) acc[u][k] = 0;
     }
     for (int j = 0; j < 4; ++j) {
+        // the x group of copy j and every group before it (all of W) are in
+        // (with hc_post in front all groups were awaited above)
         cp_async_wait(3 - j);
-        __syncthreads();  // every thread's copies of group j (j + 1 with hc_post) are in
+        __syncthreads();
         if (!active) continue;
         // unrolled, so that the loads of several feature blocks are in
         // flight together (the loop is bound by shared-memory latency)
