@@ -135,22 +135,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = (int)(blockIdx.x % kCluster);
     const int64_t F = 4LL * p.d;
-    // The W slice (row i, copy j -> W[i][j*d + r*w ...], w floats) first, one
-    // copy group per copy j, before the wait for the kernel in front: W_mix is
-    // a parameter, not an activation, so its copies overlap that kernel's tail
-    // (with programmatic dependent launch) and everything the kernel in front
-    // writes is read only after the wait.  Rows by warp, 16-byte pieces by
-    // lane: no division in the index math.
-    for (int j = 0; j < 4; ++j) {
-        const int wv = w / 4;
-        for (int i = warp; i < kMix; i += kWarps) {
-            const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
-            const uint32_t dst = su32(ws + i * nf + j * w);
-            for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
-        }
-        cp_async_commit();
-    }
-    griddep_wait_then_release();
     float *part = ws;                               // [16 warps][28][33], after the projection
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem + wreg);  // [round4(tpc)][nf]
     uint16_t *osh = reinterpret_cast<uint16_t *>(smem + wreg + xreg_bytes(w, p.tpc));  // [tpc][w]
@@ -173,7 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     // Each barrier completes once: recv when the 16 records of this CTA's
     // token are in (owners only), pre when pre of all tv tokens is in, norm
     // (with the RMSNorm) when every CTA's partial sum of y^2 of every token is,
-    // mix when the owner has put its token's mix numbers in msh.
+    // mix when the owner has put its token's mix numbers in msh.  All of it
+    // comes from the launch parameters, so it is done first, and the cluster
+    // arrival (a release) comes before any copy is in flight: a release waits
+    // for this thread's earlier memory operations, the copies included.
     if (threadIdx.x == 0) {
         *abort_word = 0;
         mbar_init(bRecv, 1);
@@ -186,6 +173,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         if (norm) mbar_expect_tx(bNorm, (uint32_t)(kCluster * tv * 4));
     }
     cluster_arrive();  // waited for before the first remote store
+
+    // The W slice (row i, copy j -> W[i][j*d + r*w ...], w floats), one copy
+    // group per copy j, before the wait for the kernel in front: W_mix is a
+    // parameter, not an activation, so its copies overlap that kernel's tail
+    // (with programmatic dependent launch) and everything the kernel in front
+    // writes is read only after the wait.  Rows by warp, 16-byte pieces by
+    // lane: no division in the index math.
+    for (int j = 0; j < 4; ++j) {
+        const int wv = w / 4;
+        for (int i = warp; i < kMix; i += kWarps) {
+            const float *src = p.w_mix + (int64_t)i * F + (int64_t)j * p.d + rank * w;
+            const uint32_t dst = su32(ws + i * nf + j * w);
+            for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
+        }
+        cp_async_commit();
+    }
+    griddep_wait_then_release();
 
     // The x slice (token t, copy j -> x[tok0+t][j][r*w ...]) follows as
     // asynchronous copies, one group per copy j after the four W groups, so
