@@ -14,9 +14,9 @@
 //     projection of copy j starts when its group is in.
 //   * Partial mix numbers and sums of squares on CUDA cores (packed
 //     two-wide fma): warp (g, h) takes tokens 4g..4g+3 and mixes 6h..6h+5
-//     over all 4w features, each lane the feature pairs 64 apart starting at
-//     2*lane; the 32 lanes' partials are then summed in lane order through
-//     shared memory.
+//     (and the squares of token 4g+h) over all 4w features, each lane the
+//     feature pairs 64 apart starting at 2*lane; the 32 lanes' partials are
+//     then summed in lane order through shared memory.
 //   * Each CTA sends its 25 partial numbers per token (24 mixes, sum of
 //     squares) to the token's owner, CTA t of the cluster for its token t,
 //     with asynchronous 4-byte stores whose bytes complete the owner's
@@ -52,7 +52,7 @@ constexpr int kRecVals = kMix + 1;    // per (sender, token): 24 mixes + sum of 
 constexpr int kRecStride = 28;        // floats between two senders' records
 constexpr int kWarps = 16;            // warp (g, h): tokens 4g.., mixes 6h..
 constexpr int kThreads = kWarps * 32;
-constexpr int kPartVals = 28;         // per warp: 4 tokens x 6 mixes + 4 sums of squares
+constexpr int kPartVals = 28;         // per warp: 4 tokens x 6 mixes + slots for 4 sums of squares
 constexpr int kPartStride = 33;       // lanes per partial value, padded: no bank conflicts
 constexpr int kMaxW = 320;            // channels per CTA (d <= 5120)
 
@@ -270,38 +270,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         }
     }
 
-    // Partial mix numbers (and sums of squares, h == 0) of tokens 4g..4g+3,
-    // as pairs (even feature, odd feature) summed at the end.
+    // Partial mix numbers of tokens 4g..4g+3 and the sum of squares of token
+    // 4g+h, as pairs (even feature, odd feature) summed at the end.  One wait
+    // for every copy group, then no barrier until the projection is done, so
+    // that the warps drift apart and one warp's shared-memory loads overlap
+    // another's FMAs (with a barrier per copy they ran in lockstep: loads,
+    // then FMAs).
     const int g = warp >> 2, h = warp & 3;
     const bool active = 4 * g < tv;
-    uint64_t acc[4][6], ssq[4];
+    uint64_t acc[4][6], ssq = 0;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        ssq[u] = 0;
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int k = 0; k < 6; ++k) acc[u][k] = 0;
-    }
-    for (int j = 0; j < 4; ++j) {
-        // the x group of copy j and every group before it (all of W) are in
-        // (with hc_post in front all groups were awaited above)
-        cp_async_wait(3 - j);
-        __syncthreads();
-        if (!active) continue;
-        // unrolled, so that the loads of several feature blocks are in
-        // flight together (the loop is bound by shared-memory latency)
+    cp_async_wait(0);
+    __syncthreads();  // every thread's copies are in
+    if (active) {
+        for (int j = 0; j < 4; ++j) {
+            // unrolled, so that the loads of several feature blocks are in
+            // flight together (the loop is bound by shared-memory latency)
 #pragma unroll 5
-        for (int f = j * w + 2 * lane; f < (j + 1) * w; f += 64) {
-            uint64_t wv[6];
+            for (int f = j * w + 2 * lane; f < (j + 1) * w; f += 64) {
+                uint64_t wv[6];
 #pragma unroll
-            for (int k = 0; k < 6; ++k)
-                wv[k] = *reinterpret_cast<const uint64_t *>(ws + (6 * h + k) * nf + f);
+                for (int k = 0; k < 6; ++k)
+                    wv[k] = *reinterpret_cast<const uint64_t *>(ws + (6 * h + k) * nf + f);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t xx = *reinterpret_cast<const uint32_t *>(xs + (4 * g + u) * nf + f);
-                const uint64_t xp = pack2(bf16lo(xx), bf16hi(xx));
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t xx =
+                        *reinterpret_cast<const uint32_t *>(xs + (4 * g + u) * nf + f);
+                    const uint64_t xp = pack2(bf16lo(xx), bf16hi(xx));
 #pragma unroll
-                for (int k = 0; k < 6; ++k) ffma2(acc[u][k], xp, wv[k]);
-                if (h == 0) ffma2(ssq[u], xp, xp);
+                    for (int k = 0; k < 6; ++k) ffma2(acc[u][k], xp, wv[k]);
+                    if (u == h) ffma2(ssq, xp, xp);
+                }
             }
         }
     }
@@ -312,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         for (int u = 0; u < 4; ++u) {
 #pragma unroll
             for (int k = 0; k < 6; ++k) pw[(u * 6 + k) * kPartStride + lane] = sum2(acc[u][k]);
-            pw[(24 + u) * kPartStride + lane] = sum2(ssq[u]);
         }
+        pw[(24 + h) * kPartStride + lane] = sum2(ssq);
     }
     __syncthreads();
     cluster_wait();  // every CTA's barriers exist and are armed
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
         const int hh = ww & 3;
         const int u = v < 24 ? v / 6 : v - 24;
         const int t = 4 * (ww >> 2) + u;
-        if (t >= tv || (v >= 24 && hh != 0)) continue;
+        if (t >= tv || (v >= 24 && hh != u)) continue;  // token u's squares: warp h = u
         const int slot = v < 24 ? 6 * hh + v % 6 : kMix;
         const float *src = part + (ww * kPartVals + v) * kPartStride;
         float s = 0.f;
