@@ -668,9 +668,21 @@ def cpu_baseline(wl, seconds):
     dt = run(k)
     k = max(16, min(wl.n, int(k * seconds / max(dt, 1e-3))))
     dt = run(k)
-    return {"value": k / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    cores = oracle.num_threads()
+    # the same on one thread, on a sample a quarter as long
+    oracle.set_num_threads(1)
+    try:
+        k1 = 16
+        dt1 = run(k1)
+        k1 = max(16, min(wl.n, int(k1 * seconds / 4 / max(dt1, 1e-3))))
+        dt1 = run(k1)
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": k / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "%d of the %d tokens (same recipe, host-drawn), full path "
-                      "mixes->Sinkhorn->pre->post in float64, %.1f s" % (k, wl.n, dt)}
+                      "mixes->Sinkhorn->pre->post in float64, %.1f s" % (k, wl.n, dt),
+            "single_thread": {"value": k1 / dt1, "unit": UNIT, "cores": 1,
+                              "sample": "%d tokens, %.1f s" % (k1, dt1)}}
 
 
 # ------------------------------------------------------------ reference arm
