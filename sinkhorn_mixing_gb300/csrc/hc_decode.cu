@@ -10,8 +10,9 @@
 //   * CTA r of a cluster owns channels [r*w, (r+1)*w) of every copy
 //     (w = d/16) and keeps its slice of W_mix (fp32, 24 x 4 x w) and of its
 //     tokens' x (bf16, tokens x 4 x w) in shared memory.
-//   * The slices arrive by asynchronous copies, one group per copy j; the
-//     projection of copy j starts when its group is in.
+//   * The slices arrive by asynchronous copies: W's before the wait for the
+//     kernel in front (W is a parameter), x's after it; the projection
+//     starts when all are in.
 //   * Partial mix numbers and sums of squares on CUDA cores (packed
 //     two-wide fma): warp (g, h) takes tokens 4g..4g+3 and mixes 6h..6h+5
 //     (and the squares of token 4g+h) over all 4w features, each lane the
@@ -96,15 +97,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
-// Wait until at most `left` of this thread's copy groups are still pending.
-__device__ __forceinline__ void cp_async_wait(int left) {
-    switch (left) {
-        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    }
+// Wait until all of this thread's copy groups are in.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 // W slice [24][4w] fp32, later reused for the lanes' partials
@@ -174,12 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     }
     cluster_arrive();  // waited for before the first remote store
 
-    // The W slice (row i, copy j -> W[i][j*d + r*w ...], w floats), one copy
-    // group per copy j, before the wait for the kernel in front: W_mix is a
-    // parameter, not an activation, so its copies overlap that kernel's tail
-    // (with programmatic dependent launch) and everything the kernel in front
-    // writes is read only after the wait.  Rows by warp, 16-byte pieces by
-    // lane: no division in the index math.
+    // The W slice (row i, copy j -> W[i][j*d + r*w ...], w floats), before
+    // the wait for the kernel in front: W_mix is a parameter, not an
+    // activation, so its copies overlap that kernel's tail (with programmatic
+    // dependent launch) and everything the kernel in front writes is read
+    // only after the wait.  Rows by warp, 16-byte pieces by lane: no division
+    // in the index math.
     for (int j = 0; j < 4; ++j) {
         const int wv = w / 4;
         for (int i = warp; i < kMix; i += kWarps) {
@@ -187,14 +182,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             const uint32_t dst = su32(ws + i * nf + j * w);
             for (int q = lane; q < wv; q += 32) cp_async16(dst + 16 * q, src + 4 * q);
         }
-        cp_async_commit();
     }
+    cp_async_commit();
     griddep_wait_then_release();
 
     // The x slice (token t, copy j -> x[tok0+t][j][r*w ...]) follows as
-    // asynchronous copies, one group per copy j after the four W groups, so
-    // that the projection of copy j starts as soon as its group is in.  Rows
-    // up to the next multiple of 4 tokens are zero.
+    // asynchronous copies.  Rows up to the next multiple of 4 tokens are zero.
     const bool post_in_front = p.out != nullptr;
     if (post_in_front) {
         // With hc_post in front the new stream needs all four copies of a
@@ -214,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
             }
         }
         cp_async_commit();
-        cp_async_wait(0);
+        cp_async_wait_all();
         __syncthreads();  // the residual and output slices (and W) are in
         // hc_post ("Mix projection" page, Block.hc_post), in the order of
         // k_post: x'_k = post_k out + sum_i comb[i][k] x_i, rounded to bf16,
@@ -266,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
                         *reinterpret_cast<uint4 *>(dst + 8 * q) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            cp_async_commit();
         }
+        cp_async_commit();
     }
 
     // Partial mix numbers of tokens 4g..4g+3 and the sum of squares of token
@@ -283,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode(const DecodeParams p) {
     for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int k = 0; k < 6; ++k) acc[u][k] = 0;
-    cp_async_wait(0);
+    cp_async_wait_all();
     __syncthreads();  // every thread's copies are in
     if (active) {
         for (int j = 0; j < 4; ++j) {
