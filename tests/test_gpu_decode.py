@@ -231,3 +231,21 @@ def test_chained_sublayers_equal_with_and_without_launch_overlap(hc, graph):
             else:
                 os.environ["HCMIX_PDL"] = old
     assert torch.equal(results[0].view(torch.int16), results[1].view(torch.int16))
+
+
+def test_new_weights_are_read_after_an_intervening_write(hc):
+    # The decode kernel copies its W slice before it waits for the kernel in
+    # front of it.  Weights rewritten on the stream before the call, with
+    # other work in between as the header requires, must still be the ones
+    # it uses.
+    n, d = 64, 5120
+    x, w, sc, base = case(n, d, 41)
+    first = run(hc, x, w, sc, base)
+    g = torch.Generator(device="cuda").manual_seed(42)
+    w.mul_(-0.5).add_(torch.randn(w.shape, device="cuda", generator=g) / (4 * d) ** 0.5)
+    scratch = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    scratch.zero_()
+    y, pre, post, comb, m, launches = run(hc, x, w, sc, base)
+    assert launches == 1, "decode path not taken"
+    assert not torch.equal(m, first[4])
+    check_all(x, w, sc, base, y, pre, post, comb, m)
