@@ -47,7 +47,8 @@
 //     x_next).
 //   * NORM (hc_mixes_pre_norm): the RMSNorm of the collapse.  The square
 //     warps also sum the ten entries G_jk = sum_c x_jc x_kc of each row's
-//     copies and store them into the owners' records; the owner forms the
+//     copies and store them, with the row's sum of squares, into the owners'
+//     records; the owner forms the
 //     collapse's sum of squares as pre^T G pre, so its RMS factor is known
 //     before the collapse writes y = bf16((bf16(sum_j pre_j x_j) g) r).
 //
@@ -82,11 +83,12 @@ constexpr int kOwn = kTM / kCluster;     // tokens owned per CTA per tile
 // the RMSNorm the 10 entries G_jk (j <= k) of the copies' Gram matrix
 constexpr int kRec = 36;
 constexpr int kGram = 10;
-// bytes of records one owner receives per tile: 16 senders x 4 tokens x 7 x 16 B
+// bytes of records one owner receives per tile: 16 senders x 4 tokens x
 // record bytes per sender and token: 6 x 16 (mixes) + 16 (sum of squares,
-// padded), or with the RMSNorm 6 x 16 + 4 + 40
+// padded), or with the RMSNorm 6 x 16 (mixes, from the read-out warps) +
+// 3 x 16 (sum of squares and Gram entries, padded, from the square warps)
 __host__ __device__ constexpr uint32_t recv_tx(bool norm) {
-    return kCluster * kOwn * (norm ? 6 * 16 + 4 + 4 * kGram : 7 * 16);
+    return kCluster * kOwn * (norm ? 9 * 16 : 7 * 16);
 }
 constexpr int kMaxNcc = 5;               // w <= 320 channels per CTA (d <= 5120)
 constexpr int kTmemCols = 128;
@@ -740,9 +742,10 @@ __global__ void __launch_bounds__(Roles<POST, NORM>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(bSqFull(b)));
             if (NORM) {
-                // the row's Gram entries go straight into its owner's record
-                // (floats 25..34), once the owner has read the previous
-                // tile's records; their bytes complete its recv_full
+                // the row's sum of squares and Gram entries go straight into
+                // its owner's record (floats 24..35), once the owner has read
+                // the previous tile's records; their bytes complete its
+                // recv_full
                 if (!__all_sync(0xFFFFFFFFu, wait_bar<true>(bar(kRecvFree), ((uint32_t)it & 1) ^ 1,
                                                             abort, p.err)))
                     break;
@@ -752,11 +755,10 @@ __global__ void __launch_bounds__(Roles<POST, NORM>::kThreads, 1)
                         mapa(su32(sm.recv + (rank * kOwn + u) * kRec), (uint32_t)owner);
                     const uint32_t rfull = mapa(bar(kRecvFull), (uint32_t)owner);
                     constexpr int g = NORM ? kGram : 1;  // (indices valid for NORM)
-                    st_async_f32(rec + 100, gs[0], rfull);
-                    st_async_v2(rec + 104, gs[1 % g], gs[2 % g], rfull);
+                    // floats 24..35: the sum of squares, G_00..G_33, a pad
+                    st_async_v4(rec + 96, ss, gs[0], gs[1 % g], gs[2 % g], rfull);
                     st_async_v4(rec + 112, gs[3 % g], gs[4 % g], gs[5 % g], gs[6 % g], rfull);
-                    st_async_v2(rec + 128, gs[7 % g], gs[8 % g], rfull);
-                    st_async_f32(rec + 136, gs[9 % g], rfull);
+                    st_async_v4(rec + 128, gs[7 % g], gs[8 % g], gs[9 % g], 0.f, rfull);
                 }
             }
         }
@@ -798,10 +800,9 @@ __global__ void __launch_bounds__(Roles<POST, NORM>::kThreads, 1)
                             acc[4 * v + 1] + acc[24 + 4 * v + 1],
                             acc[4 * v + 2] + acc[24 + 4 * v + 2],
                             acc[4 * v + 3] + acc[24 + 4 * v + 3], rfull);
-            if (NORM)
-                st_async_f32(rec + 96, ss, rfull);  // the Gram entries follow
-            else
-                st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
+            // with the RMSNorm the square warps send the sum of squares
+            // beside the Gram entries
+            if (!NORM) st_async_v4(rec + 96, ss, 0.f, 0.f, 0.f, rfull);
         }
     } else if (warp == kWarpOwner) {
         // Owner of tokens rank*kOwn + u (u < kOwn) of every tile: the 8 lanes
